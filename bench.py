@@ -1,0 +1,407 @@
+"""Benchmark of the FP8 paged-KV decode step on GB300.
+
+One step = one decode step of one layer of the workload: the batched tag
+check, the FP8 quantise-on-append of each request's new token, and the
+split-K paged decode attention with its log-sum-exp combine.  Default
+workload: 8 requests x 8,193 tokens, GQA 64/8, head_dim 128, page 16, FP8
+e4m3 cache with per-head scales, K/V ~ N(0,1) with 1 % outliers x20.
+
+Prints one JSON line.  `value` is KV-read GB/s of the whole step (algorithmic
+FP8 K+V bytes of all attended tokens / device time of the step); tokens/s,
+the fraction of HBM peak and the BF16-cache comparison ride along.
+
+  python bench.py [--steps K] [--warmup W] [--workload uniform8]
+  python bench.py --impl reference     # the CPU oracle on the same workload
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 paged decode attn: KV-read GB/s (% of HBM peak) and decode tokens/s"
+L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_uniform8.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_quantised_paged_kv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_step_runner(workload: str, seed: int = 0, requests: int = 1):
+    """The oracle on a bounded sample of the workload: its first ``requests``
+    requests, same shapes and recipe (numpy inputs, host only).
+    Returns (run_one_step, kv_bytes_per_step, cores, sub_workload)."""
+    import dataclasses
+    import oracle
+    import workloads as W
+    full = W.make(workload, seed)
+    k = min(requests, full.batch)
+    w = dataclasses.replace(full, batch=k, seq_lens=full.seq_lens[:k].copy(),
+                            block_table=full.block_table[:k].copy(),
+                            expected_tags=full.expected_tags[:k].copy())
+    hv = W.host_values(w, seed)
+    kc = np.zeros(w.cache_shape(), np.uint8)
+    vc = np.zeros(w.cache_shape(), np.uint8)
+    oracle.append(kc, vc, hv.k_prefill, hv.v_prefill, w.prefill_slot_mapping(), hv.k_scale,
+                  hv.v_scale, page_size=w.page_size)
+    slots = w.append_slot_mapping()
+
+    def run():
+        flags = oracle.tag_check(w.block_table, w.expected_tags, w.seq_lens, w.page_tags,
+                                 page_size=w.page_size)
+        oracle.append(kc, vc, hv.k_new, hv.v_new, slots, hv.k_scale, hv.v_scale, flags,
+                      page_size=w.page_size)
+        oracle.decode_attn(hv.q, kc, vc, hv.k_scale, hv.v_scale, w.block_table, w.seq_lens,
+                           w.softmax_scale, flags)
+
+    return run, w.kv_bytes(1), oracle.num_threads(), w
+
+
+def cpu_baseline(workload: str, budget_s: float = 12.0):
+    run, kv_bytes, cores, w = cpu_oracle_step_runner(workload, requests=1)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(kv_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} decode steps of {w.batch} of the {workload} requests "
+                      f"({w.kv_tokens()} tokens each step: tag check, append, attention) "
+                      f"in {dt:.1f} s, fp64 C oracle on the host CPU"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    run, kv_bytes, cores, w = cpu_oracle_step_runner(args.workload, requests=1)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = kv_bytes / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sampled_requests": w.batch,
+                   "kv_tokens_per_step": w.kv_tokens(),
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3"},
+        "tokens_per_s": round(w.batch / (ms / 1e3), 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"each step = the decode step (tag check, append, attention) "
+                                   f"of {w.batch} of the {args.workload} requests "
+                                   f"({w.kv_tokens()} tokens), fp64 C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import fp8_quantised_paged_kv_gb300 as kvq
+    import workloads as W
+    from kvq_harness import DeviceWorkload
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    kvq.load()
+    kvq.kvq_device_error(clear=True)
+
+    w = W.make(args.workload, seed=rank)
+    dw = DeviceWorkload(w, kvq.KVQ_CACHE_FP8_E4M3, device=dev)
+    ws = dw.workspace(args.num_splits)
+    out = dw.out(False)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    kv_bytes = w.kv_bytes(1)
+    split_tokens, max_splits, _ = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads,
+                                                      w.max_pages_per_seq, args.num_splits)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dw.tag_check(stream)
+        if ev is not None:
+            ev[1].record(stream)
+        dw.append(dw.abort, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        kvq.kvq_decode_attn_partial(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
+                                    dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out,
+                                    ws, args.num_splits, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        kvq.kvq_decode_attn_combine(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
+                                    dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out,
+                                    ws, args.num_splits, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    with sampler:
+        t_wall0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.zero_()                 # L2 flushed before every timed step
+                step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    parts = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                      for i in range(args.steps)])          # ms
+    step_ms = float(parts.sum(axis=1).mean())
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    tag_ms, app_ms, split_ms, comb_ms = (float(x) for x in parts.mean(axis=0))
+
+    # ---- end to end: host (pinned) inputs -> device -> step -> host result
+    host = {
+        "q": dw.q.cpu().pin_memory(), "k_new": dw.k_new.cpu().pin_memory(),
+        "v_new": dw.v_new.cpu().pin_memory(), "slots": dw.append_slots.cpu().pin_memory(),
+        "bt": dw.block_table.cpu().pin_memory(), "seq": dw.seq_lens.cpu().pin_memory(),
+        "exp": dw.expected_tags.cpu().pin_memory(),
+    }
+    dev_t = {"q": dw.q, "k_new": dw.k_new, "v_new": dw.v_new, "slots": dw.append_slots,
+             "bt": dw.block_table, "seq": dw.seq_lens, "exp": dw.expected_tags}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps + 2):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k, t in host.items():
+                dev_t[k].copy_(t, non_blocking=True)
+            step()
+            out_host.copy_(out, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            _ = float(out_host[0, 0, 0])      # the host reads the step's result
+            if i >= 2:
+                e2e_ms.append(e0.elapsed_time(e1))
+    e2e_ms_mean = float(np.mean(e2e_ms))
+
+    dev_err = kvq.kvq_device_error()
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (split_ms / 1e3) / 1e9
+    traffic = None
+    if os.path.exists(PROFILE_SUMMARY):
+        prof = json.load(open(PROFILE_SUMMARY))
+        if prof.get("source_hash") == kernel_source_hash() and prof.get("workload") == args.workload:
+            traffic = prof.get("dram_bytes_per_launch")
+
+    # BF16-cache comparison on the same workload (attention only, L2 flushed)
+    bf16_line = None
+    if not args.skip_bf16:
+        del dw
+        torch.cuda.empty_cache()
+        db = DeviceWorkload(w, kvq.KVQ_CACHE_BF16, device=dev)
+        wsb = db.workspace(args.num_splits)
+        ob = db.out(False)
+        db.append()
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                db.attend(ob, wsb, None, args.num_splits, stream)
+                b.record(stream)
+                if i >= args.warmup:
+                    times.append((a, b))
+        torch.cuda.synchronize()
+        bms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+        bf16_line = {"attn_us": round(bms * 1e3, 2), "kv_bytes": w.kv_bytes(2),
+                     "kv_gbs": round(w.kv_bytes(2) / (bms / 1e3) / 1e9, 1),
+                     "kv_bytes_per_token_per_layer": w.num_kv_heads * w.head_dim * 2 * 2,
+                     "fp8_kv_bytes_per_token_per_layer": w.num_kv_heads * w.head_dim * 2,
+                     "fp8_attn_speedup": round(bms / (split_ms + comb_ms), 3)}
+
+    if rank == 0:
+        value = world * kv_bytes / (step_ms / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch": w.batch, "kv_tokens": w.kv_tokens(),
+                       "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3",
+                       "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
+                       "l2": "flushed before every timed step (512 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "tokens_per_s": round(world * w.batch / (step_ms / 1e3), 1),
+            "hbm_frac_of_measured": round(kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
+            "kernel_us": {"tag_check": round(tag_ms * 1e3, 2), "append": round(app_ms * 1e3, 2),
+                          "decode_split": round(split_ms * 1e3, 2),
+                          "decode_combine": round(comb_ms * 1e3, 2)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "decode_split_kernel", "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": kv_bytes},
+            "e2e": {"value": round(kv_bytes / (e2e_ms_mean / 1e3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms_mean, 4), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * args.steps,
+            "bf16_cache": bf16_line,
+            "clocks": sampler.summary(),
+            "wall_s_timed_region": round(t_wall, 3),
+            "device_error_bits": dev_err,
+        }
+        if not args.skip_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="uniform8")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--skip-bf16", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,384 @@
+// kvq_abi.cu -- the extern "C" boundary declared in include/kvq.h: host-side
+// argument checks, split planning, tensor-map encoding and kernel launches.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+using kvq::kChunkTokens;
+using kvq::kHeadDim;
+
+constexpr int kMaxSplitTokens = 8192;
+constexpr int kMinAutoSplitTokens = 256;
+constexpr int kMaxSplitsTotal = 1024;
+constexpr int kCtasPerSm = 2;
+constexpr int kAutoWaves = 4;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 148;
+    if (dev < 64 && cache[dev] > 0)
+        return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev < 64)
+        cache[dev] = n;
+    return n;
+}
+
+kvq_status check_desc(const kvq_cache_desc *d)
+{
+    if (d == nullptr)
+        return KVQ_ERR_INVALID_ARG;
+    if (d->num_pages <= 0 || d->page_size <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (d->cache_dtype != KVQ_CACHE_FP8_E4M3 && d->cache_dtype != KVQ_CACHE_BF16)
+        return KVQ_ERR_INVALID_ARG;
+    if (d->head_dim != kHeadDim)
+        return KVQ_ERR_UNSUPPORTED;
+    if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64 && d->page_size != 128)
+        return KVQ_ERR_UNSUPPORTED;
+    // tensor-copy row coordinates are 32-bit: rows of 128 bytes in one cache
+    const int64_t lines = static_cast<int64_t>(d->num_pages) * d->num_kv_heads * d->page_size *
+                          (d->cache_dtype == KVQ_CACHE_BF16 ? 2 : 1);
+    if (lines > 0x7FFFFFFFLL)
+        return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+struct Plan {
+    int32_t split_tokens, max_splits;
+    size_t lse_bytes, o_bytes;
+};
+
+kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads,
+                     int32_t max_pages, int32_t num_splits, Plan *p)
+{
+    kvq_status st = check_desc(d);
+    if (st != KVQ_OK)
+        return st;
+    if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_q_heads % d->num_kv_heads != 0)
+        return KVQ_ERR_INVALID_ARG;
+    const int g = num_q_heads / d->num_kv_heads;
+    if (g > kvq::kMaxGroup)
+        return KVQ_ERR_UNSUPPORTED;
+    const int64_t max_ctx = static_cast<int64_t>(max_pages) * d->page_size;
+    const int64_t unit = d->page_size > kChunkTokens ? d->page_size : kChunkTokens;
+    int64_t want;
+    if (num_splits > 0) {
+        want = num_splits;
+    } else {
+        const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kAutoWaves;
+        const int64_t work = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads * max_ctx;
+        int64_t per = (work + target - 1) / target;
+        if (per < kMinAutoSplitTokens)
+            per = kMinAutoSplitTokens;
+        want = (max_ctx + per - 1) / per;
+    }
+    if (want < 1)
+        want = 1;
+    int64_t split = (max_ctx + want - 1) / want;
+    split = (split + unit - 1) / unit * unit;
+    if (split > kMaxSplitTokens)
+        split = kMaxSplitTokens;
+    int64_t splits = (max_ctx + split - 1) / split;
+    if (splits > kMaxSplitsTotal)
+        return KVQ_ERR_UNSUPPORTED;
+    p->split_tokens = static_cast<int32_t>(split);
+    p->max_splits = static_cast<int32_t>(splits);
+    if (splits > 1) {
+        const size_t n = static_cast<size_t>(batch) * num_q_heads * splits;
+        p->lse_bytes = (n * sizeof(float) + 255) / 256 * 256;
+        p->o_bytes = n * kHeadDim * sizeof(float);
+    } else {
+        p->lse_bytes = p->o_bytes = 0;
+    }
+    return KVQ_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link libcuda directly.
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn()
+{
+    static EncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(p);
+    });
+    return fn;
+}
+
+bool make_cache_map(CUtensorMap *map, const kvq_cache_desc *d, const void *cache)
+{
+    EncodeFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
+    const cuuint64_t rows = static_cast<cuuint64_t>(d->num_pages) * d->num_kv_heads *
+                            d->page_size * (bf16 ? 2 : 1);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(bf16 ? 64 : 128), rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(bf16 ? 64 : 128),
+                               static_cast<cuuint32_t>(kvq::tma_box_rows(d->page_size, bf16))};
+    const cuuint32_t estr[2] = {1, 1};
+    std::memset(map, 0, sizeof *map);
+    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          2, const_cast<void *>(cache), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+kvq_status to_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+struct DecodeCall {
+    kvq::DecodeArgs args;
+    Plan plan;
+};
+
+kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                          int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                          const float *k_scale, const float *v_scale, const int32_t *block_table,
+                          int32_t max_pages_per_seq, const int32_t *seq_lens, float softmax_scale,
+                          const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                          void *workspace, size_t workspace_bytes, int32_t num_splits,
+                          DecodeCall *call)
+{
+    kvq_status st = make_plan(desc, batch, num_q_heads, max_pages_per_seq, num_splits, &call->plan);
+    if (st != KVQ_OK)
+        return st;
+    if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_FP32)
+        return KVQ_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale))
+        return KVQ_ERR_INVALID_ARG;
+    const bool bf16 = desc->cache_dtype == KVQ_CACHE_BF16;
+    if (batch > 0) {
+        if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+            return KVQ_ERR_INVALID_ARG;
+        if (!bf16 && (!k_scale || !v_scale))
+            return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+            return KVQ_ERR_INVALID_ARG;
+    }
+    if (batch > 65535)
+        return KVQ_ERR_UNSUPPORTED;
+    const size_t need = call->plan.lse_bytes + call->plan.o_bytes;
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return KVQ_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace))
+        return KVQ_ERR_INVALID_ARG;
+    kvq::DecodeArgs &a = call->args;
+    a.q = q;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.abort_flags = abort_flags;
+    a.out = out;
+    a.ws_lse = need > 0 ? static_cast<float *>(workspace) : nullptr;
+    a.ws_o = need > 0 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                   call->plan.lse_bytes)
+                      : nullptr;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.group = num_q_heads / desc->num_kv_heads;
+    a.page_size = desc->page_size;
+    a.num_pages = desc->num_pages;
+    a.max_pages_per_seq = max_pages_per_seq;
+    a.split_tokens = call->plan.split_tokens;
+    a.max_splits = call->plan.max_splits;
+    a.qk_scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.out_fp32 = out_dtype == KVQ_OUT_FP32;
+    a.bf16_cache = bf16;
+    return KVQ_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *kvq_status_string(kvq_status s)
+{
+    switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape";
+    case KVQ_ERR_WORKSPACE: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+kvq_status kvq_append(const kvq_cache_desc *desc, const void *k_new, const void *v_new,
+                      const int64_t *slot_mapping, int32_t num_tokens, const float *k_scale,
+                      const float *v_scale, const uint8_t *abort_flags, void *k_cache,
+                      void *v_cache, kvq_stream_t stream)
+{
+    kvq_status st = check_desc(desc);
+    if (st != KVQ_OK)
+        return st;
+    if (num_tokens < 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return KVQ_OK;
+    const bool bf16 = desc->cache_dtype == KVQ_CACHE_BF16;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+        return KVQ_ERR_INVALID_ARG;
+    if (!bf16 && (!k_scale || !v_scale))
+        return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return KVQ_ERR_INVALID_ARG;
+    kvq::AppendArgs a;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slot_mapping = slot_mapping;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.abort_flags = abort_flags;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_tokens = num_tokens;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.page_size = desc->page_size;
+    a.num_slots = static_cast<int64_t>(desc->num_pages) * desc->page_size;
+    a.bf16_cache = bf16;
+    return to_status(kvq::launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_tag_check(const int32_t *block_table, const uint32_t *expected_tags,
+                         const int32_t *seq_lens, int32_t batch, int32_t max_pages_per_seq,
+                         int32_t page_size, const uint32_t *page_tags, int32_t num_pages,
+                         uint8_t *abort_flags, kvq_stream_t stream)
+{
+    if (batch < 0 || max_pages_per_seq <= 0 || page_size <= 0 || num_pages <= 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (batch == 0)
+        return KVQ_OK;
+    if (!block_table || !expected_tags || !seq_lens || !page_tags || !abort_flags)
+        return KVQ_ERR_INVALID_ARG;
+    kvq::TagCheckArgs a;
+    a.block_table = block_table;
+    a.expected_tags = expected_tags;
+    a.seq_lens = seq_lens;
+    a.page_tags = page_tags;
+    a.abort_flags = abort_flags;
+    a.batch = batch;
+    a.max_pages_per_seq = max_pages_per_seq;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    return to_status(kvq::launch_tag_check(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
+                           int32_t max_pages_per_seq, int32_t num_splits, int32_t *split_tokens,
+                           int32_t *max_splits, size_t *workspace_bytes)
+{
+    Plan p;
+    kvq_status st = make_plan(desc, batch, num_q_heads, max_pages_per_seq, num_splits, &p);
+    if (st != KVQ_OK)
+        return st;
+    if (split_tokens)
+        *split_tokens = p.split_tokens;
+    if (max_splits)
+        *max_splits = p.max_splits;
+    if (workspace_bytes)
+        *workspace_bytes = p.lse_bytes + p.o_bytes;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn_partial(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, int32_t max_pages_per_seq,
+                                   const int32_t *seq_lens, float softmax_scale,
+                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
+                                   kvq_stream_t stream)
+{
+    DecodeCall call;
+    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
+                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
+                                   num_splits, &call);
+    if (st != KVQ_OK || batch == 0)
+        return st;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
+        return KVQ_ERR_CUDA;
+    return to_status(kvq::launch_decode_partial(call.args, km, vm,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_attn_combine(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, int32_t max_pages_per_seq,
+                                   const int32_t *seq_lens, float softmax_scale,
+                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
+                                   kvq_stream_t stream)
+{
+    DecodeCall call;
+    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
+                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
+                                   num_splits, &call);
+    if (st != KVQ_OK || batch == 0)
+        return st;
+    return to_status(kvq::launch_decode_combine(call.args, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                           int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                           const float *k_scale, const float *v_scale, const int32_t *block_table,
+                           int32_t max_pages_per_seq, const int32_t *seq_lens, float softmax_scale,
+                           const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                           void *workspace, size_t workspace_bytes, int32_t num_splits,
+                           kvq_stream_t stream)
+{
+    DecodeCall call;
+    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
+                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
+                                   num_splits, &call);
+    if (st != KVQ_OK || batch == 0)
+        return st;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
+        return KVQ_ERR_CUDA;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = kvq::launch_decode_partial(call.args, km, vm, s);
+    if (e != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return to_status(kvq::launch_decode_combine(call.args, s));
+}
+
+kvq_status kvq_device_error(uint32_t *bits, int32_t clear)
+{
+    return to_status(kvq::read_device_error(bits, clear != 0));
+}
+
+} // extern "C"

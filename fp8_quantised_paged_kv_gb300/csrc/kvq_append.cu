@@ -1,0 +1,88 @@
+// kvq_append.cu -- quantise-on-append of new K/V tokens into the paged cache.
+//
+// The cache is kept as FP8 e4m3 instead of BF16, halving its size (blog post
+// "Smaller, faster, safer: running Kimi and GLM at scale", page-1 mirror,
+// section "量化KV缓存").  Each element becomes e4m3(x / scale[h]): the
+// division is one IEEE fp32 round-to-nearest operation and the conversion
+// rounds to nearest even and saturates at +-448 (cvt ... .satfinite).
+//
+// One row = one (token, K|V, KV head) vector of 128 elements; 16 threads per
+// row, each loading 16 bytes (8 bf16) and storing 8 bytes (8 codes), so both
+// the bf16 source and the paged destination are accessed fully coalesced.
+#include "kvq_internal.h"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreadsPerRow = kHeadDim / 8;   // 16
+constexpr int kAppendThreads = 256;
+
+template <bool kBf16Cache>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a)
+{
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (kAppendThreads / kThreadsPerRow) +
+                        threadIdx.x / kThreadsPerRow;
+    const int part = threadIdx.x % kThreadsPerRow;
+    const int64_t rows = static_cast<int64_t>(a.num_tokens) * 2 * a.num_kv_heads;
+    if (row >= rows)
+        return;
+    const int64_t t = row / (2 * a.num_kv_heads);
+    const int rem = static_cast<int>(row % (2 * a.num_kv_heads));
+    const bool is_v = rem >= a.num_kv_heads;
+    const int h = is_v ? rem - a.num_kv_heads : rem;
+
+    if (a.abort_flags != nullptr && a.abort_flags[t] != 0)
+        return;
+    const int64_t slot = a.slot_mapping[t];
+    if (slot < 0 || slot >= a.num_slots)
+        return;
+    const int64_t page = slot / a.page_size;
+    const int64_t off = slot % a.page_size;
+    const int64_t dst_row = (page * a.num_kv_heads + h) * a.page_size + off;
+
+    const uint16_t *src = static_cast<const uint16_t *>(is_v ? a.v_new : a.k_new) +
+                          (t * a.num_kv_heads + h) * kHeadDim + part * 8;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src));
+
+    if constexpr (kBf16Cache) {
+        uint16_t *dst = static_cast<uint16_t *>(is_v ? a.v_cache : a.k_cache) +
+                        dst_row * kHeadDim + part * 8;
+        *reinterpret_cast<uint4 *>(dst) = x;
+    } else {
+        const float scale = (is_v ? a.v_scale : a.k_scale)[h];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t packed[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float2 p0 = bf16x2_to_f32x2(w[2 * i]);
+            const float2 p1 = bf16x2_to_f32x2(w[2 * i + 1]);
+            const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(p0.x, scale), __fdiv_rn(p0.y, scale));
+            const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(p1.x, scale), __fdiv_rn(p1.y, scale));
+            packed[i] = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+        }
+        uint8_t *dst = static_cast<uint8_t *>(is_v ? a.v_cache : a.k_cache) +
+                       dst_row * kHeadDim + part * 8;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream)
+{
+    const int64_t rows = static_cast<int64_t>(a.num_tokens) * 2 * a.num_kv_heads;
+    if (rows == 0)
+        return cudaSuccess;
+    const int64_t rows_per_block = kAppendThreads / kThreadsPerRow;
+    const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+    if (blocks > 0x7FFFFFFF)
+        return cudaErrorInvalidValue;
+    if (a.bf16_cache)
+        append_kernel<true><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(a);
+    else
+        append_kernel<false><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace kvq

@@ -1,0 +1,614 @@
+// kvq_decode.cu -- single-token paged decode attention over an FP8 e4m3 (or
+// BF16) KV cache, split along the context, plus the log-sum-exp combine.
+//
+// What it computes (blog post "Smaller, faster, safer: running Kimi and GLM
+// at scale", page-1 mirror section "量化KV缓存"; page-3 mirror section
+// "FP8 省的不仅是显存"): decode attention whose kernel converts the FP8
+// values it reads.  For query head h of request r, KV head kvh = h / g:
+//   out = sum_j exp(s_j - max s) V^_j / sum_j exp(s_j - max s),
+//   s_j = softmax_scale * <q, K^_j>,  K^ = e4m3 value * k_scale[kvh].
+//
+// Split kernel: one CTA per (split, KV head, request) covers every query
+// head of the group, so each cache byte is fetched from HBM and converted
+// once.  Four warps; each warp owns every 4th 32-token chunk of the split
+// and a private 3-stage ring of shared-memory tiles filled by 2-D tensor
+// bulk copies (TMA, 128-byte swizzle) that an mbarrier per stage tracks.
+// Per chunk the warp runs, on the tensor cores (mma.sync m16n8k16, f16 in,
+// fp32 accumulate), S^T = K Q^T with tokens as M and the g <= 8 query heads
+// as N, an fp32 online softmax, and O^T += V^T P^T.  e4m3 codes become f16
+// in registers (exact); movmatrix turns the score fragment into the PV
+// operand.  The four warps merge in shared memory; a request that fits in
+// one split gets its final output here, longer ones write (lse, o) partials
+// that the combine kernel merges.
+#include <cfloat>
+
+#include <cuda_bf16.h>
+
+#include "kvq_internal.h"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+
+// Sticky device error word (bit 0: a bulk-copy wait timed out).
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // give up on a copy after ~1 s
+constexpr int kCombineThreads = 128;
+constexpr int kMaxSplits = 1024;
+
+template <bool kBf16Cache>
+struct Tile {
+    static constexpr int kRowBytes = kBf16Cache ? 256 : 128;      // one token of one head
+    static constexpr int kBytes = kChunkTokens * kRowBytes;       // K (or V) part of a stage
+    static constexpr int kStages = kBf16Cache ? 2 : 3;
+    static constexpr int kStageBytes = 2 * kBytes;
+    static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes +
+                                      kWarps * kStages * 8 /* barriers */ + kMaxPageList * 4 + 16;
+};
+
+// Byte offset of 16-byte chunk `c` of 128-byte line `line` in a tile written
+// by a 128-byte-swizzled tensor copy into a 1024-byte-aligned buffer.
+__device__ __forceinline__ uint32_t swz(int line, int c)
+{
+    return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t *base, uint32_t off)
+{
+    return *reinterpret_cast<const uint4 *>(base + off);
+}
+
+__device__ __forceinline__ float warp_max_over_rows(float v)
+{
+    // lanes that share lane % 4 hold the same query heads
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 8));
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 16));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_over_rows(float v)
+{
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+    return v;
+}
+
+__device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool fp32)
+{
+    if (fp32)
+        static_cast<float *>(out)[idx] = v;
+    else
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+template <bool kBf16Cache, bool kPreciseP>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
+                    const __grid_constant__ CUtensorMap v_map, const DecodeArgs a)
+{
+    using T = Tile<kBf16Cache>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
+    int32_t *page_list = reinterpret_cast<int32_t *>(full + kWarps * T::kStages);
+    __shared__ int s_failed;
+
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int g = a.group, ps = a.page_size;
+    const int hq0 = kvh * g;                               // first query head of the group
+
+    const int64_t len = a.seq_lens[b];
+    const bool aborted = a.abort_flags != nullptr && a.abort_flags[b] != 0;
+    const int64_t cap = static_cast<int64_t>(a.max_pages_per_seq) * ps;
+    const bool zero_request = aborted || len <= 0 || len > cap;
+    const int nsplit = zero_request ? 1 : static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
+    if (split >= nsplit)
+        return;
+
+    if (zero_request) {                                    // split 0 writes the zeros
+        for (int i = threadIdx.x; i < g * kHeadDim; i += kThreads)
+            store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + hq0) * kHeadDim + i, 0.f,
+                      a.out_fp32);
+        return;
+    }
+
+    const int64_t t0 = static_cast<int64_t>(split) * a.split_tokens;
+    const int64_t t1 = min(len, t0 + a.split_tokens);
+    // page ids of this split (t0 is a multiple of the page size)
+    const int first_page = static_cast<int>(t0 / ps);
+    const int n_pages = static_cast<int>((t1 - 1) / ps) - first_page + 1;
+    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
+    bool bad = false;
+    for (int i = threadIdx.x; i < n_pages; i += kThreads) {
+        const int32_t p = bt[i];
+        bad |= (p < 0 || p >= a.num_pages);
+        page_list[i] = p;
+    }
+    if (threadIdx.x == 0) {
+        s_failed = 0;
+        for (int i = 0; i < kWarps * T::kStages; ++i)
+            mbar_init(&full[i], 1);
+        fence_mbar_init();
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (nsplit == 1) {
+            for (int i = threadIdx.x; i < g * kHeadDim; i += kThreads)
+                store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + hq0) * kHeadDim + i,
+                          0.f, a.out_fp32);
+        } else if (threadIdx.x < g) {
+            a.ws_lse[(static_cast<int64_t>(b) * a.num_q_heads + hq0 + threadIdx.x) * a.max_splits +
+                     split] = __int_as_float(0x7FC00000);   // NaN marks an invalid split
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- setup
+    const int n_chunks = static_cast<int>((t1 - t0 + kChunkTokens - 1) / kChunkTokens);
+    const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
+    uint8_t *ring = smem + warp * T::kStages * T::kStageBytes;
+    uint64_t *my_full = full + warp * T::kStages;
+    const int box_tok = ps < kChunkTokens ? ps : kChunkTokens;
+    const int parts = kChunkTokens / box_tok;                       // 1 or 2 copies per tensor
+    const int lines_per_tok = kBf16Cache ? 2 : 1;
+    const uint32_t part_bytes = static_cast<uint32_t>(box_tok * T::kRowBytes);
+    const uint64_t policy = l2_policy_evict_first();
+
+    if (lane == 0) {
+        prefetch_tensor_map(&k_map);
+        prefetch_tensor_map(&v_map);
+    }
+
+    // Issue the copies of this warp's local chunk `it` (lane 0 only).
+    auto issue = [&](int it) {
+        const int c = warp + it * kWarps;
+        const int64_t tok = t0 + static_cast<int64_t>(c) * kChunkTokens;
+        const int st = it % T::kStages;
+        uint8_t *kdst = ring + st * T::kStageBytes;
+        uint8_t *vdst = kdst + T::kBytes;
+        int np = 0;
+        int32_t ys[2];
+        for (int part = 0; part < parts; ++part) {
+            const int64_t ptok = tok + part * box_tok;
+            if (ptok >= t1)
+                break;
+            const int32_t page = page_list[static_cast<int>(ptok / ps) - first_page];
+            const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + ptok % ps;
+            ys[np++] = static_cast<int32_t>(row * lines_per_tok);
+        }
+        mbar_arrive_expect_tx(&my_full[st], 2u * part_bytes * np);
+        for (int i = 0; i < np; ++i) {
+            tma_load_2d(kdst + i * part_bytes, &k_map, 0, ys[i], &my_full[st], policy);
+            tma_load_2d(vdst + i * part_bytes, &v_map, 0, ys[i], &my_full[st], policy);
+        }
+    };
+
+    if (lane == 0) {
+        const int pro = my_chunks < T::kStages ? my_chunks : T::kStages;
+        for (int it = 0; it < pro; ++it)
+            issue(it);
+    }
+
+    // Query fragments (mma B operand): lane (gq, tq) holds query head gq of
+    // the group at dims 32*tq .. 32*tq+31; k-slot pairs of k-step c map to
+    // dims 32*tq + 4*c + {0,1} and {2,3}.
+    uint32_t qf[8][2];
+    {
+        uint32_t w[16];
+        if (gq < g) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const uint16_t *>(a.q) +
+                ((static_cast<int64_t>(b) * a.num_q_heads + hq0 + gq) * kHeadDim + 32 * tq));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = __ldg(src + i);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                w[i] = 0;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if constexpr (kBf16Cache) {
+                    qf[c][j] = w[2 * c + j];
+                } else {
+                    const float2 f = bf16x2_to_f32x2(w[2 * c + j]);
+                    qf[c][j] = f32x2_to_f16x2(f.x, f.y);
+                }
+            }
+        }
+    }
+
+    const float kscale = kBf16Cache ? 1.f : a.k_scale[kvh];
+    const float vscale = kBf16Cache ? 1.f : a.v_scale[kvh];
+    const float qk_scale = a.qk_scale_log2 * kscale;
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    bool failed = false;
+    int it = 0;
+    for (; it < my_chunks; ++it) {
+        const int st = it % T::kStages;
+        if (!mbar_wait_bounded(&my_full[st], (it / T::kStages) & 1, kWaitLimitNs)) {
+            failed = true;
+            break;
+        }
+        const uint8_t *ks = ring + st * T::kStageBytes;
+        const uint8_t *vs = ks + T::kBytes;
+        const int c = warp + it * kWarps;
+        const int64_t tok = t0 + static_cast<int64_t>(c) * kChunkTokens;
+        const int64_t left = t1 - tok;
+        const int n_valid = left < kChunkTokens ? static_cast<int>(left) : kChunkTokens;
+
+        // ---- S^T = K Q^T for the two 16-token m-tiles
+        float sc[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+            const int r0 = mt * 16 + gq, r1 = r0 + 8;
+            if constexpr (kBf16Cache) {
+                uint32_t w0[16], w1[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int line0 = 2 * r0 + (tq >> 1), line1 = 2 * r1 + (tq >> 1);
+                    const uint4 x0 = lds128(ks, swz(line0, (tq & 1) * 4 + j));
+                    const uint4 x1 = lds128(ks, swz(line1, (tq & 1) * 4 + j));
+                    w0[4 * j] = x0.x; w0[4 * j + 1] = x0.y; w0[4 * j + 2] = x0.z; w0[4 * j + 3] = x0.w;
+                    w1[4 * j] = x1.x; w1[4 * j + 1] = x1.y; w1[4 * j + 2] = x1.z; w1[4 * j + 3] = x1.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(sc[mt], w0[2 * kk], w1[2 * kk], w0[2 * kk + 1], w1[2 * kk + 1],
+                             qf[kk][0], qf[kk][1]);
+            } else {
+                const uint4 x0a = lds128(ks, swz(r0, 2 * tq)), x0b = lds128(ks, swz(r0, 2 * tq + 1));
+                const uint4 x1a = lds128(ks, swz(r1, 2 * tq)), x1b = lds128(ks, swz(r1, 2 * tq + 1));
+                const uint32_t w0[8] = {x0a.x, x0a.y, x0a.z, x0a.w, x0b.x, x0b.y, x0b.z, x0b.w};
+                const uint32_t w1[8] = {x1a.x, x1a.y, x1a.z, x1a.w, x1b.x, x1b.y, x1b.z, x1b.w};
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16(sc[mt], lo16_e4m3x2_to_f16x2(w0[kk]), lo16_e4m3x2_to_f16x2(w1[kk]),
+                            hi16_e4m3x2_to_f16x2(w0[kk]), hi16_e4m3x2_to_f16x2(w1[kk]),
+                            qf[kk][0], qf[kk][1]);
+            }
+        }
+
+        // ---- online softmax (log2 domain); lane holds heads 2tq, 2tq+1
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = mt * 16 + gq + ((i & 2) ? 8 : 0);
+                float x = sc[mt][i] * qk_scale;
+                x = row < n_valid ? x : -INFINITY;
+                sc[mt][i] = x;
+                mx[i & 1] = fmaxf(mx[i & 1], x);
+            }
+        }
+        float alpha[2], base[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float mnew = fmaxf(m_run[j], warp_max_over_rows(mx[j]));
+            base[j] = mnew == -INFINITY ? 0.f : mnew;
+            alpha[j] = fast_exp2(m_run[j] - base[j]);
+            m_run[j] = mnew;
+        }
+        float psum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float p = fast_exp2(sc[mt][i] - base[i & 1]);
+                sc[mt][i] = p;
+                psum[i & 1] += p;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            l_run[j] = l_run[j] * alpha[j] + psum[j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i][0] *= alpha[0];
+            o[i][1] *= alpha[1];
+            o[i][2] *= alpha[0];
+            o[i][3] *= alpha[1];
+        }
+
+        // ---- O^T += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            uint32_t x0, x1;
+            if constexpr (kBf16Cache) {
+                x0 = f32x2_to_bf16x2(sc[mt][0], sc[mt][1]);
+                x1 = f32x2_to_bf16x2(sc[mt][2], sc[mt][3]);
+            } else {
+                x0 = f32x2_to_f16x2(sc[mt][0], sc[mt][1]);
+                x1 = f32x2_to_f16x2(sc[mt][2], sc[mt][3]);
+            }
+            const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
+            uint32_t pl0 = 0, pl1 = 0;
+            if constexpr (kPreciseP) {
+                // second term carries what the 16-bit rounding of P dropped
+                const float2 h0 = kBf16Cache ? bf16x2_to_f32x2(x0) : f16x2_to_f32x2(x0);
+                const float2 h1 = kBf16Cache ? bf16x2_to_f32x2(x1) : f16x2_to_f32x2(x1);
+                const uint32_t y0 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y)
+                                               : f32x2_to_f16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y);
+                const uint32_t y1 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y)
+                                               : f32x2_to_f16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y);
+                pl0 = movmatrix_trans(y0);
+                pl1 = movmatrix_trans(y1);
+            }
+            // V rows of token slots 2tq, 2tq+1, 2tq+8, 2tq+9 of this m-tile
+            const int rv = mt * 16 + 2 * tq;
+            const int rows[4] = {rv, rv + 1, rv + 8, rv + 9};
+            if constexpr (kBf16Cache) {
+                uint32_t R[4][8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int line = 2 * rows[q] + (gq >> 2);
+                    const uint4 lo = lds128(vs, swz(line, (gq & 3) * 2));
+                    const uint4 hi = lds128(vs, swz(line, (gq & 3) * 2 + 1));
+                    const bool keep = rows[q] < n_valid;
+                    R[q][0] = keep ? lo.x : 0u; R[q][1] = keep ? lo.y : 0u;
+                    R[q][2] = keep ? lo.z : 0u; R[q][3] = keep ? lo.w : 0u;
+                    R[q][4] = keep ? hi.x : 0u; R[q][5] = keep ? hi.y : 0u;
+                    R[q][6] = keep ? hi.z : 0u; R[q][7] = keep ? hi.w : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t a0 = prmt(R[0][i], R[1][i], 0x5410);
+                    const uint32_t a1 = prmt(R[0][i], R[1][i], 0x7632);
+                    const uint32_t a2 = prmt(R[2][i], R[3][i], 0x5410);
+                    const uint32_t a3 = prmt(R[2][i], R[3][i], 0x7632);
+                    mma_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
+                    if constexpr (kPreciseP)
+                        mma_bf16(o[i], a0, a1, a2, a3, pl0, pl1);
+                }
+            } else {
+                uint32_t R[4][4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = lds128(vs, swz(rows[q], gq));
+                    const bool keep = rows[q] < n_valid;
+                    R[q][0] = keep ? v.x : 0u; R[q][1] = keep ? v.y : 0u;
+                    R[q][2] = keep ? v.z : 0u; R[q][3] = keep ? v.w : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                    const uint32_t p01 = prmt(R[0][i >> 1], R[1][i >> 1], sel);
+                    const uint32_t p23 = prmt(R[2][i >> 1], R[3][i >> 1], sel);
+                    const uint32_t a0 = lo16_e4m3x2_to_f16x2(p01), a1 = hi16_e4m3x2_to_f16x2(p01);
+                    const uint32_t a2 = lo16_e4m3x2_to_f16x2(p23), a3 = hi16_e4m3x2_to_f16x2(p23);
+                    mma_f16(o[i], a0, a1, a2, a3, pb0, pb1);
+                    if constexpr (kPreciseP)
+                        mma_f16(o[i], a0, a1, a2, a3, pl0, pl1);
+                }
+            }
+        }
+
+        // ---- refill this stage with the chunk kStages ahead
+        __syncwarp();
+        if (lane == 0 && it + T::kStages < my_chunks) {
+            fence_proxy_async_smem();
+            issue(it + T::kStages);
+        }
+    }
+
+    if (failed) {
+        // drain the copies this warp still has in flight, then leave
+        if (lane == 0) {
+            atomicOr(&g_device_error, 1u);
+            s_failed = 1;
+        }
+        const int issued = my_chunks < it + T::kStages ? my_chunks : it + T::kStages;
+        for (int j = it + 1; j < issued; ++j)
+            mbar_wait_bounded(&my_full[j % T::kStages], (j / T::kStages) & 1, kWaitLimitNs);
+    }
+    __syncthreads();
+    if (s_failed)
+        return;
+
+    // ---- merge the four warps' states in shared memory (ring is free now)
+    float *sm_o = reinterpret_cast<float *>(smem);                     // [kWarps][8][128]
+    float *sm_m = sm_o + kWarps * kMaxGroup * kHeadDim;               // [kWarps][8]
+    float *sm_l = sm_m + kWarps * kMaxGroup;                          // [kWarps][8]
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        l_run[j] = warp_sum_over_rows(l_run[j]);
+    {
+        float *ow = sm_o + warp * kMaxGroup * kHeadDim;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int d = 16 * gq + 2 * i;
+            *reinterpret_cast<float2 *>(ow + (2 * tq) * kHeadDim + d) = make_float2(o[i][0], o[i][2]);
+            *reinterpret_cast<float2 *>(ow + (2 * tq + 1) * kHeadDim + d) = make_float2(o[i][1], o[i][3]);
+        }
+        if (gq == 0) {
+            sm_m[warp * kMaxGroup + 2 * tq] = m_run[0];
+            sm_m[warp * kMaxGroup + 2 * tq + 1] = m_run[1];
+            sm_l[warp * kMaxGroup + 2 * tq] = l_run[0];
+            sm_l[warp * kMaxGroup + 2 * tq + 1] = l_run[1];
+        }
+    }
+    __syncthreads();
+
+    const int d = threadIdx.x;                                          // kThreads == kHeadDim
+    for (int h = 0; h < g; ++h) {
+        float mmax = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            mmax = fmaxf(mmax, sm_m[w * kMaxGroup + h]);
+        float lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = sm_m[w * kMaxGroup + h];
+            const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - mmax);
+            lsum += sm_l[w * kMaxGroup + h] * f;
+            acc += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * f;
+        }
+        const float val = acc / lsum * vscale;
+        const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + hq0 + h;
+        if (nsplit == 1) {
+            store_out(a.out, bh * kHeadDim + d, val, a.out_fp32);
+        } else {
+            a.ws_o[(bh * a.max_splits + split) * kHeadDim + d] = val;
+            if (d == 0)
+                a.ws_lse[bh * a.max_splits + split] = mmax + __log2f(lsum);
+        }
+    }
+}
+
+// One CTA per (query head, request): merge the split partials by their
+// log-sum-exp weights.  Requests that fit in one split were finished by the
+// split kernel and are skipped here.
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeArgs a)
+{
+    __shared__ float s_w[kMaxSplits];
+    __shared__ float s_red[kCombineThreads / 32];
+    __shared__ int s_bad;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int64_t len = a.seq_lens[b];
+    const bool aborted = a.abort_flags != nullptr && a.abort_flags[b] != 0;
+    const int64_t cap = static_cast<int64_t>(a.max_pages_per_seq) * a.page_size;
+    if (aborted || len <= 0 || len > cap)
+        return;
+    const int nsplit = static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
+    if (nsplit <= 1)
+        return;
+    const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + h;
+    const float *lse = a.ws_lse + bh * a.max_splits;
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    if (tid == 0)
+        s_bad = 0;
+    __syncthreads();
+
+    float mloc = -INFINITY;
+    for (int s = tid; s < nsplit; s += kCombineThreads) {
+        const float v = lse[s];
+        if (v != v)
+            s_bad = 1;
+        s_w[s] = v;
+        mloc = fmaxf(mloc, v);
+    }
+    for (int off = 16; off > 0; off >>= 1)
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xFFFFFFFFu, mloc, off));
+    if (lane == 0)
+        s_red[warp] = mloc;
+    __syncthreads();
+    float mmax = s_red[0];
+    for (int w = 1; w < kCombineThreads / 32; ++w)
+        mmax = fmaxf(mmax, s_red[w]);
+    const bool bad = s_bad != 0;
+    __syncthreads();
+
+    float wsum = 0.f;
+    for (int s = tid; s < nsplit; s += kCombineThreads) {
+        const float w = bad ? 0.f : fast_exp2(s_w[s] - mmax);
+        s_w[s] = w;
+        wsum += w;
+    }
+    for (int off = 16; off > 0; off >>= 1)
+        wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, off);
+    if (lane == 0)
+        s_red[warp] = wsum;
+    __syncthreads();
+    float total = 0.f;
+    for (int w = 0; w < kCombineThreads / 32; ++w)
+        total += s_red[w];
+
+    for (int d = tid; d < kHeadDim; d += kCombineThreads) {
+        float acc = 0.f;
+        if (!bad) {
+            const float *ob = a.ws_o + bh * a.max_splits * kHeadDim + d;
+            for (int s = 0; s < nsplit; ++s)
+                acc += s_w[s] * ob[static_cast<int64_t>(s) * kHeadDim];
+            acc /= total;
+        }
+        store_out(a.out, bh * kHeadDim + d, acc, a.out_fp32);
+    }
+}
+
+template <bool kBf16, bool kPrecise>
+cudaError_t launch_split(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                         cudaStream_t stream)
+{
+    using T = Tile<kBf16>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(decode_split_kernel<kBf16, kPrecise>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = 1;
+    }
+    const dim3 grid(static_cast<unsigned>(a.max_splits), static_cast<unsigned>(a.num_kv_heads),
+                    static_cast<unsigned>(a.batch));
+    decode_split_kernel<kBf16, kPrecise><<<grid, kThreads, T::kSmemBytes, stream>>>(k_map, v_map, a);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_decode_partial(const DecodeArgs &a, const CUtensorMap &k_map,
+                                  const CUtensorMap &v_map, cudaStream_t stream)
+{
+    if (a.batch == 0)
+        return cudaSuccess;
+    if (a.bf16_cache)
+        return a.out_fp32 ? launch_split<true, true>(a, k_map, v_map, stream)
+                          : launch_split<true, false>(a, k_map, v_map, stream);
+    return a.out_fp32 ? launch_split<false, true>(a, k_map, v_map, stream)
+                      : launch_split<false, false>(a, k_map, v_map, stream);
+}
+
+cudaError_t launch_decode_combine(const DecodeArgs &a, cudaStream_t stream)
+{
+    if (a.batch == 0 || a.max_splits <= 1)
+        return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(a.num_q_heads), static_cast<unsigned>(a.batch));
+    decode_combine_kernel<<<grid, kCombineThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(uint32_t *bits, bool clear)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess)
+        return e;
+    if (bits)
+        *bits = v;
+    if (clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    }
+    return e;
+}
+
+} // namespace kvq

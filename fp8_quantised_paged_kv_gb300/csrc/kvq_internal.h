@@ -1,0 +1,71 @@
+// kvq_internal.h -- launch interfaces shared by the C ABI (kvq_abi.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+constexpr int kChunkTokens = 32;     // tokens one warp consumes per pipeline stage
+constexpr int kMaxGroup = 8;         // query heads per KV head on one mma n-tile
+
+struct AppendArgs {
+    const void *k_new, *v_new;       // bf16 [T][Hkv][D]
+    const int64_t *slot_mapping;     // [T]
+    const float *k_scale, *v_scale;  // [Hkv]
+    const uint8_t *abort_flags;      // [T] or null
+    void *k_cache, *v_cache;
+    int32_t num_tokens, num_kv_heads, page_size;
+    int64_t num_slots;               // num_pages * page_size
+    bool bf16_cache;
+};
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
+
+struct TagCheckArgs {
+    const int32_t *block_table;
+    const uint32_t *expected_tags;
+    const int32_t *seq_lens;
+    const uint32_t *page_tags;
+    uint8_t *abort_flags;
+    int32_t batch, max_pages_per_seq, page_size, num_pages;
+};
+cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream);
+
+// Workspace layout (bytes from the workspace base):
+//   [0, lse_bytes)           fp32 lse[B][Hq][S]  (log2-domain, NaN = invalid split)
+//   [o_offset, +o_bytes)     fp32 o[B][Hq][S][D]  (each split's normalised output)
+struct DecodeArgs {
+    const void *q;                   // bf16 [B][Hq][D]
+    const float *k_scale, *v_scale;  // [Hkv] (unused for bf16 cache)
+    const int32_t *block_table;      // [B][max_pages]
+    const int32_t *seq_lens;         // [B]
+    const uint8_t *abort_flags;      // [B] or null
+    void *out;                       // [B][Hq][D]
+    float *ws_lse;
+    float *ws_o;
+    int32_t batch, num_q_heads, num_kv_heads, group, page_size, num_pages;
+    int32_t max_pages_per_seq, split_tokens, max_splits;
+    float qk_scale_log2;             // softmax_scale * log2(e)
+    bool out_fp32, bf16_cache;
+};
+
+// Split kernel + combine kernel.  The tensor maps describe the K and V
+// caches as 2-D [rows][128 bytes] tensors with 128-byte swizzle.
+cudaError_t launch_decode_partial(const DecodeArgs &a, const CUtensorMap &k_map,
+                                  const CUtensorMap &v_map, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeArgs &a, cudaStream_t stream);
+
+// Box height (in 128-byte rows) of one bulk copy for a page size.
+inline int tma_box_rows(int page_size, bool bf16_cache)
+{
+    int tok = page_size < kChunkTokens ? page_size : kChunkTokens;
+    return bf16_cache ? 2 * tok : tok;
+}
+
+cudaError_t read_device_error(uint32_t *bits, bool clear);
+
+} // namespace kvq

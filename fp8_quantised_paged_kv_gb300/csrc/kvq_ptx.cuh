@@ -1,0 +1,212 @@
+// kvq_ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels:
+// e4m3 <-> f16 / f32 conversion, mma.sync m16n8k16, movmatrix, mbarrier,
+// and 2-D tensor bulk copies (TMA) into shared memory.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- formats
+
+// Two e4m3 codes (low byte = element 0) -> f16x2 (low half = element 0).
+// Every e4m3 value is exactly representable in f16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two_codes)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two_codes));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lo16_e4m3x2_to_f16x2(uint32_t w)
+{
+    return e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu));
+}
+
+__device__ __forceinline__ uint32_t hi16_e4m3x2_to_f16x2(uint32_t w)
+{
+    return e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+
+// Two fp32 values -> two e4m3 codes, round to nearest even, saturating to
+// +-448.  Element 0 lands in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float e0, float e1)
+{
+    uint16_t r;
+    // the first source operand fills the upper byte
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(e1), "f"(e0));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v)
+{
+    uint16_t lo = static_cast<uint16_t>(v & 0xFFFFu), hi = static_cast<uint16_t>(v >> 16);
+    float a, b;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(a) : "h"(lo));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(b) : "h"(hi));
+    return make_float2(a, b);
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t v)
+{
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// ------------------------------------------------------------ tensor core
+
+// D += A * B, m16n8k16, f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with bf16 inputs.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Warp-wide transpose of an 8x8 matrix of 16-bit elements held in the
+// mma accumulator layout (lane holds row lane/4, columns 2*(lane%4) + {0,1}).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// --------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of the barrier to complete, giving up after about
+// `limit_ns` nanoseconds (and after 2^30 polls in any case).  Returns false
+// on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    uint64_t start = global_timer_ns();
+    for (uint32_t i = 0; i < (1u << 30); ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 255u) == 255u && global_timer_ns() - start > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+// ------------------------------------------------------------------- TMA
+
+// 2-D tiled bulk copy global -> shared, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tensor_map, int32_t x,
+                                            int32_t y, uint64_t *bar, uint64_t l2_policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(smem_addr(bar)),
+        "l"(l2_policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tensor_map(const void *tensor_map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tensor_map))
+                 : "memory");
+}
+
+} // namespace kvq

@@ -1,0 +1,237 @@
+/*
+ * kvq.h -- C ABI of the FP8 paged-KV decode path for GB300 (sm_103a).
+ *
+ * Three operations, each one hand-written CUDA kernel family:
+ *
+ *   kvq_tag_check    per-page integrity tags: the separate batched check that
+ *                    runs before decode reads the cache and aborts a request
+ *                    whose pages changed owner.  Source: blog post "Smaller,
+ *                    faster, safer: running Kimi and GLM at scale" (page-2
+ *                    mirror, section "KV Cache 完整性检查"; page-3 mirror,
+ *                    section "一个不能出错的共享缓存").
+ *   kvq_append       quantise-on-append: each new token's BF16 K and V
+ *                    stored as FP8 e4m3 (or kept as BF16) in its paged slot.
+ *                    Source: page-1 mirror, section "量化KV缓存" (the cache
+ *                    is stored as FP8 e4m3 instead of BF16, halving its size).
+ *   kvq_decode_attn  single-token paged attention over the cache, converting
+ *                    FP8 values on read, split across CTAs along the context
+ *                    and merged with a log-sum-exp combine.  Source: page-1
+ *                    mirror, section "量化KV缓存" (the FP8 attention kernel
+ *                    converts the values it reads); page-3 mirror, section
+ *                    "FP8 省的不仅是显存".
+ *
+ * Argument dimensions follow the KV-size formula of the page-4 article
+ * (section "显存为什么会成为长上下文推理的瓶颈"): requests x tokens x
+ * layers x KV heads x head_dim x {K, V} x bytes per element.  One call
+ * handles one layer; a multi-layer model calls once per layer with that
+ * layer's caches and scales (page ids and tags are shared by all layers).
+ *
+ * Common rules
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise and
+ *     must be 16-byte aligned.  The caller owns every buffer, including the
+ *     decode workspace; the library allocates no device memory.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream).  Argument checks are made on the host before anything is
+ *     launched and are returned synchronously; a failed launch returns
+ *     KVQ_ERR_CUDA.
+ *   - Bad DATA never traps: an out-of-range slot is skipped by append; a page
+ *     id outside [0, num_pages) or a request longer than its block-table row
+ *     aborts the request in the tag check and makes decode write zeros for
+ *     it without reading any page.
+ *   - Cache layout (page-major): cache[num_pages][num_kv_heads][page_size]
+ *     [head_dim], 1 byte per element (e4m3 codes) or 2 (bf16).  Each
+ *     (page, KV head) tile is one contiguous run of page_size * head_dim
+ *     elements.  A token at logical position j of request r lives in page
+ *     block_table[r][j / page_size], slot j % page_size.
+ *   - Supported: head_dim 128; page_size 16, 32, 64 or 128; query heads per
+ *     KV head (g = num_q_heads / num_kv_heads) 1 to 8.  Others return
+ *     KVQ_ERR_UNSUPPORTED.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+struct CUstream_st;
+/* The same handle as cudaStream_t / CUstream. */
+typedef struct CUstream_st *kvq_stream_t;
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    KVQ_ERR_UNSUPPORTED = 2,   /* shape outside the supported set above */
+    KVQ_ERR_WORKSPACE = 3,     /* decode workspace smaller than kvq_decode_plan says */
+    KVQ_ERR_CUDA = 4           /* a CUDA runtime call or launch failed */
+} kvq_status;
+
+typedef enum { KVQ_CACHE_FP8_E4M3 = 0, KVQ_CACHE_BF16 = 1 } kvq_cache_dtype;
+typedef enum { KVQ_OUT_BF16 = 0, KVQ_OUT_FP32 = 1 } kvq_out_dtype;
+
+/* Shape of one layer's K cache (the V cache has the same shape). */
+typedef struct {
+    int32_t num_pages;     /* physical pages N in the pool */
+    int32_t page_size;     /* tokens per page */
+    int32_t num_kv_heads;  /* Hkv */
+    int32_t head_dim;      /* D */
+    int32_t cache_dtype;   /* kvq_cache_dtype */
+} kvq_cache_desc;
+
+/*
+ * kvq_append -- write T new tokens' K and V into their cache slots.
+ *
+ *   k_new, v_new   bf16 [T][Hkv][D], token-major.
+ *   slot_mapping   int64 [T]; token t goes to page slot_mapping[t] / page_size,
+ *                  slot slot_mapping[t] % page_size.  A slot < 0 or >= N *
+ *                  page_size skips the token (no write, no error).
+ *   k_scale, v_scale  fp32 [Hkv], this layer's per-KV-head scales (K and V
+ *                  separate).  FP8 cache: code = e4m3(x / scale), the
+ *                  division one IEEE fp32 round-to-nearest operation, the
+ *                  conversion round-to-nearest-even and saturating at
+ *                  +-448 (a NaN input stays NaN).  Ignored (may be NULL) for
+ *                  the bf16 cache, which stores x unchanged.
+ *   abort_flags    uint8 [T] or NULL: a non-zero flag skips token t (in a
+ *                  decode step token t belongs to request t).
+ *   k_cache, v_cache  the caches described by *desc; only the addressed
+ *                  slots are written.
+ * Two tokens mapped to the same slot race; the caller must not do that.
+ */
+KVQ_API kvq_status kvq_append(const kvq_cache_desc *desc, const void *k_new, const void *v_new,
+                      const int64_t *slot_mapping, int32_t num_tokens,
+                      const float *k_scale, const float *v_scale,
+                      const uint8_t *abort_flags, void *k_cache, void *v_cache,
+                      kvq_stream_t stream);
+
+/*
+ * kvq_tag_check -- the separate batched integrity pass, run before decode
+ * reads the cache.
+ *
+ *   block_table    int32 [B][max_pages_per_seq], physical page of each of a
+ *                  request's logical pages.
+ *   expected_tags  uint32 [B][max_pages_per_seq], the tag each request
+ *                  recorded for each of its pages when it was given the page.
+ *   seq_lens       int32 [B], tokens of each request (entries beyond
+ *                  ceil(seq_lens[r] / page_size) are ignored).
+ *   page_tags      uint32 [num_pages], the live tag of every physical page
+ *                  (the allocator changes it whenever the page is reassigned).
+ *   abort_flags    uint8 [B], OUTPUT: 1 if any used entry names a page
+ *                  outside [0, num_pages), a page whose live tag differs from
+ *                  the expected one, or if the request needs more entries than
+ *                  its row has; else 0.  Every flag is written.
+ * Pass the flags to kvq_append and kvq_decode_attn of the same step.  A
+ * deployment that does not want the check skips this call and passes NULL
+ * flags (the no-op tracker of the page-3 article: zero cost).
+ */
+KVQ_API kvq_status kvq_tag_check(const int32_t *block_table, const uint32_t *expected_tags,
+                         const int32_t *seq_lens, int32_t batch, int32_t max_pages_per_seq,
+                         int32_t page_size, const uint32_t *page_tags, int32_t num_pages,
+                         uint8_t *abort_flags, kvq_stream_t stream);
+
+/*
+ * kvq_decode_plan -- HOST-only query: how kvq_decode_attn will split the
+ * context and how many workspace bytes it needs.
+ *
+ *   num_splits     requested splits per (request, KV head); 0 = automatic
+ *                  (sized from the device's SM count and the batch).
+ *   *split_tokens  OUT: tokens per split (a multiple of 32).
+ *   *max_splits    OUT: splits of the longest possible request,
+ *                  ceil(max_pages_per_seq * page_size / *split_tokens).
+ *   *workspace_bytes OUT: bytes of workspace kvq_decode_attn needs
+ *                  (0 when no request can need more than one split).
+ * Any OUT pointer may be NULL.
+ */
+KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
+                           int32_t max_pages_per_seq, int32_t num_splits,
+                           int32_t *split_tokens, int32_t *max_splits,
+                           size_t *workspace_bytes);
+
+/*
+ * kvq_decode_attn -- single-token attention for B requests over the paged
+ * cache, computed as:
+ *   for query head h of request r (KV head kvh = h / g):
+ *     s_j = softmax_scale * <q[r][h], K^_j>,   j = 0 .. seq_lens[r] - 1
+ *     out[r][h] = sum_j exp(s_j - max s) V^_j / sum_j exp(s_j - max s)
+ *   with K^ = e4m3 value * k_scale[kvh] (bf16 cache: the bf16 value), same
+ *   for V.
+ *
+ *   q              bf16 [B][Hq][D].  On the FP8 path q is used in f16, which
+ *                  is exact for |q| in [2^-14, 65504]; smaller magnitudes lose
+ *                  relative precision (absolute error < 2^-25) and larger
+ *                  ones overflow.
+ *   k_cache, v_cache, desc  as in kvq_append.
+ *   k_scale, v_scale  fp32 [Hkv] (ignored, may be NULL, for the bf16 cache).
+ *   block_table, max_pages_per_seq, seq_lens  as in kvq_tag_check.
+ *   abort_flags    uint8 [B] or NULL; a set flag gives zeros and no reads.
+ *   out            [B][Hq][D], bf16 or fp32 per out_dtype.  Requests that are
+ *                  aborted, empty (seq_len <= 0), longer than their table row
+ *                  or that name a page outside [0, num_pages) get zeros.
+ *   workspace      device scratch of at least the kvq_decode_plan size for
+ *                  the same arguments (NULL allowed when that size is 0);
+ *                  holds the per-split partial results between the split
+ *                  kernel and the combine kernel of this call.  Two calls in
+ *                  flight at once must not share it.
+ *   num_splits     as in kvq_decode_plan.
+ * Launches the split kernel and, when some request spans more than one
+ * split, the log-sum-exp combine kernel.
+ */
+KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                           int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *block_table, int32_t max_pages_per_seq,
+                           const int32_t *seq_lens, float softmax_scale,
+                           const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                           void *workspace, size_t workspace_bytes, int32_t num_splits,
+                           kvq_stream_t stream);
+
+/*
+ * The two halves of kvq_decode_attn, for callers that want to place other
+ * work (or timing events) between them.  Same arguments; call partial, then
+ * combine, on the same stream with the same workspace.  partial writes the
+ * final output of every request that fits in one split (and the zeros of
+ * aborted, empty or invalid ones); combine merges the rest.
+ */
+KVQ_API kvq_status kvq_decode_attn_partial(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, int32_t max_pages_per_seq,
+                                   const int32_t *seq_lens, float softmax_scale,
+                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
+                                   kvq_stream_t stream);
+KVQ_API kvq_status kvq_decode_attn_combine(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, int32_t max_pages_per_seq,
+                                   const int32_t *seq_lens, float softmax_scale,
+                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
+                                   kvq_stream_t stream);
+
+/*
+ * kvq_device_error -- HOST call, synchronous: reads (into *bits, host
+ * memory) and, if `clear` is non-zero, resets the sticky device error word
+ * of the current device.  Bit 0: a bulk-copy wait in the decode split kernel
+ * gave up after its time limit (about one second); the kernel then drained
+ * its copies and returned without writing that CTA's results.  0 means no
+ * such event since the last clear.
+ */
+KVQ_API kvq_status kvq_device_error(uint32_t *bits, int32_t clear);
+
+/* Static, human-readable name of a status code. */
+KVQ_API const char *kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/kvq.h declares, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_quantised_paged_kv_gb300 as kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]*?\b(kvq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared()
+    for n in ("kvq_append", "kvq_tag_check", "kvq_decode_attn", "kvq_decode_plan",
+              "kvq_status_string"):
+        assert n in names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = kvq.load()
+    for name in declared():
+        assert hasattr(lib, name), name
+    assert set(declared()) <= set(kvq.EXPORTED)
+
+
+def test_status_strings():
+    assert kvq.kvq_status_string(0) == "ok"
+    assert kvq.kvq_status_string(3) == "workspace too small"
+
+
+def _plan(ps=16, hkv=8, B=8, hq=64, maxp=513, splits=0, dtype=0, head_dim=128):
+    desc = kvq.CacheDesc(4104, ps, hkv, head_dim, dtype)
+    return kvq.kvq_decode_plan(desc, B, hq, maxp, splits)
+
+
+def test_plan_splits_cover_the_context():
+    for ps in (16, 32, 64, 128):
+        for maxp in (1, 2, 33, 513, 4096):
+            for splits in (0, 1, 3, 64):
+                st, ms, ws = _plan(ps=ps, maxp=maxp, splits=splits)
+                ctx = maxp * ps
+                assert st % 32 == 0 and st % min(ps, 32) == 0 and st % ps == 0 and st <= 8192
+                assert ms == -(-ctx // st)
+                assert (ws == 0) == (ms == 1)
+                if splits:
+                    assert ms <= max(splits, -(-ctx // 8192))
+
+
+def test_plan_rejects_unsupported_shapes():
+    with pytest.raises(kvq.KvqError) as e:
+        _plan(head_dim=64)
+    assert e.value.status == 2
+    with pytest.raises(kvq.KvqError) as e:
+        _plan(ps=8)
+    assert e.value.status == 2
+    with pytest.raises(kvq.KvqError) as e:
+        _plan(hq=16 * 8)          # g = 16
+    assert e.value.status == 2
+    with pytest.raises(kvq.KvqError) as e:
+        _plan(hq=63)              # not a multiple of Hkv
+    assert e.value.status == 1
+
+
+def test_calls_with_null_pointers_fail_on_the_host():
+    lib = kvq.load()
+    desc = kvq.CacheDesc(64, 16, 8).c()
+    st = lib.kvq_append(ctypes.byref(desc), None, None, None, 4, None, None, None, None, None, None)
+    assert st == 1
+    st = lib.kvq_tag_check(None, None, None, 4, 8, 16, None, 64, None, None)
+    assert st == 1
+    st = lib.kvq_decode_attn(ctypes.byref(desc), None, 2, 8, None, None, None, None, None, 8,
+                             None, ctypes.c_float(0.1), None, None, 0, None, 0, 0, None)
+    assert st == 1
+    # zero-sized work is a no-op
+    assert lib.kvq_append(ctypes.byref(desc), None, None, None, 0, None, None, None, None, None,
+                          None) == 0
+    assert lib.kvq_tag_check(None, None, None, 0, 8, 16, None, 64, None, None) == 0
+
+
+def test_misaligned_pointer_rejected():
+    lib = kvq.load()
+    desc = kvq.CacheDesc(64, 16, 8).c()
+    p = ctypes.c_void_p(0x1000 + 8)
+    st = lib.kvq_append(ctypes.byref(desc), p, p, p, 4, p, p, None, p, p, None)
+    assert st == 1
+
+
+def test_workspace_too_small_is_reported():
+    lib = kvq.load()
+    desc = kvq.CacheDesc(4104, 16, 8).c()
+    p = ctypes.c_void_p(0x10000)
+    st = lib.kvq_decode_attn(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p,
+                             ctypes.c_float(0.1), None, p, 0, p, 16, 0, None)
+    assert st == 3

@@ -125,9 +125,11 @@ class Workload:
                                for r, L in enumerate(self.seq_lens)]).astype(np.int64)
 
     def append_slot_mapping(self) -> np.ndarray:
-        """Slot of each request's appended token (position L-1)."""
-        return np.array([self.slots_of(r, [int(L) - 1])[0] for r, L in enumerate(self.seq_lens)],
-                        dtype=np.int64)
+        """Slot of each request's appended token (position L-1); -1 (skip) if the
+        request is empty or longer than its block-table row."""
+        cap = self.block_table.shape[1] * self.page_size
+        return np.array([self.slots_of(r, [int(L) - 1])[0] if 0 < L <= cap else -1
+                         for r, L in enumerate(self.seq_lens)], dtype=np.int64)
 
     def kv_tokens(self) -> int:
         return int(np.sum(self.seq_lens))
@@ -205,6 +207,20 @@ def make(name: str, seed: int = 0, *, scale_down: int = 1) -> Workload:
     return Workload(name, B, Hq, Hkv, D, ps, N, seq, bt, page_tags, expected,
                     1.0 / math.sqrt(D), seed, outlier_frac=outl,
                     num_layers=32 if name == "churn" else 1)
+
+
+def make_custom(lens, *, group: int, page_size: int, num_kv_heads: int = 2, seed: int = 0,
+                pool_factor: float = 1.5, outlier_frac: float = 0.0, name: str = "custom") -> Workload:
+    """A small workload with the given per-request lengths (test cases)."""
+    rng = np.random.default_rng(seed)
+    seq = np.asarray(lens, dtype=np.int32)
+    demand = sum(max(-(-int(L) // page_size), 1) for L in seq)
+    N = int(math.ceil(pool_factor * demand)) + 1
+    bt = _tables(rng, np.maximum(seq, 1), page_size, N)
+    page_tags, expected = _tags(rng, N, bt)
+    D = 128
+    return Workload(name, len(seq), num_kv_heads * group, num_kv_heads, D, page_size, N, seq, bt,
+                    page_tags, expected, 1.0 / math.sqrt(D), seed, outlier_frac=outlier_frac)
 
 
 CHURN_STEPS = 100
