@@ -8,22 +8,21 @@
 // (blog post "Smaller, faster, safer", page-2 mirror section "KV Cache
 // 完整性检查"; page-3 mirror section "一个不能出错的共享缓存").
 //
-// One warp per request scans the ceil(L / page_size) entries it uses with
-// coalesced loads of the block-table and expected-tag rows, gathers the live
-// tags, and OR-reduces with __any_sync.  Lane 0 writes the flag (0 or 1).
+// One CTA per request: its threads take the ceil(L / page_size) entries the
+// request uses in one strided pass (coalesced block-table and expected-tag
+// loads, one gather of the live tag each), OR-reduce with __syncthreads_or,
+// and thread 0 writes the flag (0 or 1).  A 513-page request costs one round
+// of dependent loads instead of 17 rounds on a single warp.
 #include "kvq_internal.h"
 
 namespace kvq {
 namespace {
 
-constexpr int kTagThreads = 256;
+constexpr int kTagThreads = 128;
 
 __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
 {
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * (kTagThreads / 32) + warp;
-    if (r >= a.batch)
-        return;
+    const int64_t r = blockIdx.x;
     const int64_t len = a.seq_lens[r] > 0 ? a.seq_lens[r] : 0;
     int64_t used = (len + a.page_size - 1) / a.page_size;
     bool bad = false;
@@ -33,13 +32,14 @@ __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
     }
     const int32_t *bt = a.block_table + r * a.max_pages_per_seq;
     const uint32_t *exp = a.expected_tags + r * a.max_pages_per_seq;
-    for (int64_t i = lane; i < used; i += 32) {
+    for (int64_t i = threadIdx.x; i < used; i += kTagThreads) {
         const int32_t p = __ldg(bt + i);
-        if (p < 0 || p >= a.num_pages || __ldg(a.page_tags + p) != __ldg(exp + i))
+        const uint32_t want = __ldg(exp + i);
+        if (p < 0 || p >= a.num_pages || __ldg(a.page_tags + p) != want)
             bad = true;
     }
-    bad = __any_sync(0xFFFFFFFFu, bad);
-    if (lane == 0)
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0)
         a.abort_flags[r] = bad ? 1 : 0;
 }
 
@@ -49,9 +49,7 @@ cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream)
 {
     if (a.batch == 0)
         return cudaSuccess;
-    const int per_block = kTagThreads / 32;
-    const unsigned blocks = static_cast<unsigned>((a.batch + per_block - 1) / per_block);
-    tag_check_kernel<<<blocks, kTagThreads, 0, stream>>>(a);
+    tag_check_kernel<<<static_cast<unsigned>(a.batch), kTagThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -204,8 +204,12 @@ def test_decode_edge_requests_zeroed():
     w.seq_lens[4] = w.block_table.shape[1] * 16 + 3  # longer than its table row
     abort = np.zeros(len(lens), np.uint8)
     abort[5] = 1
+    rng = np.random.default_rng(4)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
     for splits in (1, 0, 4):
         dw = DeviceWorkload(w, kvq.KVQ_CACHE_FP8_E4M3, populate=False)
+        dw.k_cache.copy_(torch.from_numpy(rng.choice(finite, size=w.cache_shape()).astype(np.uint8)))
+        dw.v_cache.copy_(torch.from_numpy(rng.choice(finite, size=w.cache_shape()).astype(np.uint8)))
         dw.q.normal_()
         out = dw.out(True)
         out.fill_(123.0)
