@@ -164,10 +164,10 @@ def kvq_decode_plan(desc: CacheDesc, batch: int, num_q_heads: int, max_pages_per
 
 
 def workspace_for(desc: CacheDesc, batch, num_q_heads, max_pages_per_seq, num_splits=0, device="cuda"):
-    """Allocate (with torch) the decode workspace the plan asks for, or None."""
+    """Allocate (with torch) the zero-filled decode workspace the plan asks for."""
     import torch
     nbytes = kvq_decode_plan(desc, batch, num_q_heads, max_pages_per_seq, num_splits)[2]
-    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
 def _decode(fn_name, desc: CacheDesc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,

@@ -13,10 +13,10 @@ using kvq::kChunkTokens;
 using kvq::kHeadDim;
 
 constexpr int kMaxSplitTokens = 8192;
-constexpr int kMinAutoSplitTokens = 256;
+constexpr int kMinAutoSplitTokens = 512;
 constexpr int kMaxSplitsTotal = 1024;
-constexpr int kCtasPerSm = 2;
-constexpr int kAutoWaves = 4;
+constexpr int kCtasPerSm = 2;          // resident CTAs of the persistent split kernel per SM
+constexpr int kUnitsPerCta = 8;        // the automatic split size aims at this many units per CTA
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -57,7 +57,7 @@ kvq_status check_desc(const kvq_cache_desc *d)
 }
 
 struct Plan {
-    int32_t split_tokens, max_splits;
+    int32_t split_tokens, max_splits, grid;
     size_t lse_bytes, o_bytes;
 };
 
@@ -69,6 +69,8 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         return st;
     if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0)
         return KVQ_ERR_INVALID_ARG;
+    if (batch > kvq::decode_max_batch())
+        return KVQ_ERR_UNSUPPORTED;
     if (num_q_heads % d->num_kv_heads != 0)
         return KVQ_ERR_INVALID_ARG;
     const int g = num_q_heads / d->num_kv_heads;
@@ -80,7 +82,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (num_splits > 0) {
         want = num_splits;
     } else {
-        const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kAutoWaves;
+        const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kUnitsPerCta;
         const int64_t work = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads * max_ctx;
         int64_t per = (work + target - 1) / target;
         if (per < kMinAutoSplitTokens)
@@ -98,6 +100,9 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         return KVQ_ERR_UNSUPPORTED;
     p->split_tokens = static_cast<int32_t>(split);
     p->max_splits = static_cast<int32_t>(splits);
+    const int64_t units = static_cast<int64_t>(batch) * d->num_kv_heads * splits;
+    const int64_t slots = static_cast<int64_t>(sm_count()) * kCtasPerSm;
+    p->grid = static_cast<int32_t>(units < slots ? (units > 0 ? units : 1) : slots);
     if (splits > 1) {
         const size_t n = static_cast<size_t>(batch) * num_q_heads * splits;
         p->lse_bytes = (n * sizeof(float) + 255) / 256 * 256;
@@ -184,10 +189,10 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     }
     if (batch > 65535)
         return KVQ_ERR_UNSUPPORTED;
-    const size_t need = call->plan.lse_bytes + call->plan.o_bytes;
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    const size_t need = kvq::kCounterBytes + call->plan.lse_bytes + call->plan.o_bytes;
+    if (workspace == nullptr || workspace_bytes < need)
         return KVQ_ERR_WORKSPACE;
-    if (need > 0 && !aligned16(workspace))
+    if (!aligned16(workspace))
         return KVQ_ERR_INVALID_ARG;
     kvq::DecodeArgs &a = call->args;
     a.q = q;
@@ -197,10 +202,12 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     a.seq_lens = seq_lens;
     a.abort_flags = abort_flags;
     a.out = out;
-    a.ws_lse = need > 0 ? static_cast<float *>(workspace) : nullptr;
-    a.ws_o = need > 0 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                                   call->plan.lse_bytes)
-                      : nullptr;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.counters = reinterpret_cast<unsigned int *>(ws);
+    a.ws_lse = call->plan.lse_bytes ? reinterpret_cast<float *>(ws + kvq::kCounterBytes) : nullptr;
+    a.ws_o = call->plan.o_bytes
+                 ? reinterpret_cast<float *>(ws + kvq::kCounterBytes + call->plan.lse_bytes)
+                 : nullptr;
     a.batch = batch;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = desc->num_kv_heads;
@@ -305,7 +312,7 @@ kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t nu
     if (max_splits)
         *max_splits = p.max_splits;
     if (workspace_bytes)
-        *workspace_bytes = p.lse_bytes + p.o_bytes;
+        *workspace_bytes = kvq::kCounterBytes + p.lse_bytes + p.o_bytes;
     return KVQ_OK;
 }
 
@@ -329,7 +336,8 @@ kvq_status kvq_decode_attn_partial(const kvq_cache_desc *desc, const void *q, in
     if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
         return KVQ_ERR_CUDA;
     return to_status(kvq::launch_decode_partial(call.args, km, vm,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+                                                reinterpret_cast<cudaStream_t>(stream),
+                                                call.plan.grid));
 }
 
 kvq_status kvq_decode_attn_combine(const kvq_cache_desc *desc, const void *q, int32_t batch,
@@ -370,7 +378,7 @@ kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t ba
     if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
         return KVQ_ERR_CUDA;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = kvq::launch_decode_partial(call.args, km, vm, s);
+    cudaError_t e = kvq::launch_decode_partial(call.args, km, vm, s, call.plan.grid);
     if (e != cudaSuccess)
         return KVQ_ERR_CUDA;
     return to_status(kvq::launch_decode_combine(call.args, s));

@@ -36,8 +36,11 @@ struct TagCheckArgs {
 cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream);
 
 // Workspace layout (bytes from the workspace base):
-//   [0, lse_bytes)           fp32 lse[B][Hq][S]  (log2-domain, NaN = invalid split)
-//   [o_offset, +o_bytes)     fp32 o[B][Hq][S][D]  (each split's normalised output)
+//   [0, 256)                 uint32 counters[2]: next work unit, finished CTAs
+//                            (zero before the first call; every call leaves them zero)
+//   [256, +lse_bytes)        fp32 lse[B][Hq][S]  (log2 domain, NaN = invalid split)
+//   [.., +o_bytes)           fp32 o[B][Hq][S][D]  (each split's normalised output)
+constexpr size_t kCounterBytes = 256;
 struct DecodeArgs {
     const void *q;                   // bf16 [B][Hq][D]
     const float *k_scale, *v_scale;  // [Hkv] (unused for bf16 cache)
@@ -45,6 +48,7 @@ struct DecodeArgs {
     const int32_t *seq_lens;         // [B]
     const uint8_t *abort_flags;      // [B] or null
     void *out;                       // [B][Hq][D]
+    unsigned int *counters;
     float *ws_lse;
     float *ws_o;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, num_pages;
@@ -56,7 +60,8 @@ struct DecodeArgs {
 // Split kernel + combine kernel.  The tensor maps describe the K and V
 // caches as 2-D [rows][128 bytes] tensors with 128-byte swizzle.
 cudaError_t launch_decode_partial(const DecodeArgs &a, const CUtensorMap &k_map,
-                                  const CUtensorMap &v_map, cudaStream_t stream);
+                                  const CUtensorMap &v_map, cudaStream_t stream, int grid);
+int decode_max_batch();
 cudaError_t launch_decode_combine(const DecodeArgs &a, cudaStream_t stream);
 
 // Box height (in 128-byte rows) of one bulk copy for a page size.

@@ -44,8 +44,8 @@
  *     elements.  A token at logical position j of request r lives in page
  *     block_table[r][j / page_size], slot j % page_size.
  *   - Supported: head_dim 128; page_size 16, 32, 64 or 128; query heads per
- *     KV head (g = num_q_heads / num_kv_heads) 1 to 8.  Others return
- *     KVQ_ERR_UNSUPPORTED.
+ *     KV head (g = num_q_heads / num_kv_heads) 1 to 8; up to 1024 requests
+ *     per decode call.  Others return KVQ_ERR_UNSUPPORTED.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -146,8 +146,9 @@ KVQ_API kvq_status kvq_tag_check(const int32_t *block_table, const uint32_t *exp
  *   *split_tokens  OUT: tokens per split (a multiple of 32).
  *   *max_splits    OUT: splits of the longest possible request,
  *                  ceil(max_pages_per_seq * page_size / *split_tokens).
- *   *workspace_bytes OUT: bytes of workspace kvq_decode_attn needs
- *                  (0 when no request can need more than one split).
+ *   *workspace_bytes OUT: bytes of workspace kvq_decode_attn needs: a
+ *                  256-byte scheduling header plus, when a request can span
+ *                  more than one split, the per-split partial results.
  * Any OUT pointer may be NULL.
  */
 KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
@@ -176,10 +177,12 @@ KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, in
  *                  aborted, empty (seq_len <= 0), longer than their table row
  *                  or that name a page outside [0, num_pages) get zeros.
  *   workspace      device scratch of at least the kvq_decode_plan size for
- *                  the same arguments (NULL allowed when that size is 0);
- *                  holds the per-split partial results between the split
- *                  kernel and the combine kernel of this call.  Two calls in
- *                  flight at once must not share it.
+ *                  the same arguments.  Its first 256 bytes are the work
+ *                  counters of the persistent split kernel: they must be zero
+ *                  before the first call that uses the buffer, and every call
+ *                  leaves them zero again.  The rest holds the per-split
+ *                  partial results between the split and combine kernels of
+ *                  one call.  Two calls in flight at once must not share it.
  *   num_splits     as in kvq_decode_plan.
  * Launches the split kernel and, when some request spans more than one
  * split, the log-sum-exp combine kernel.

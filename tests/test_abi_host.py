@@ -50,7 +50,7 @@ def test_plan_splits_cover_the_context():
                 ctx = maxp * ps
                 assert st % 32 == 0 and st % min(ps, 32) == 0 and st % ps == 0 and st <= 8192
                 assert ms == -(-ctx // st)
-                assert (ws == 0) == (ms == 1)
+                assert (ws == 256) == (ms == 1)      # the 256-byte counter header is always there
                 if splits:
                     assert ms <= max(splits, -(-ctx // 8192))
 
@@ -101,3 +101,12 @@ def test_workspace_too_small_is_reported():
     st = lib.kvq_decode_attn(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p,
                              ctypes.c_float(0.1), None, p, 0, p, 16, 0, None)
     assert st == 3
+    st = lib.kvq_decode_attn(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p,
+                             ctypes.c_float(0.1), None, p, 0, None, 1 << 30, 0, None)
+    assert st == 3                      # the counter header is always needed
+
+
+def test_batch_limit():
+    with pytest.raises(kvq.KvqError) as e:
+        _plan(B=1025)
+    assert e.value.status == 2
