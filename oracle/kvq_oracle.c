@@ -157,7 +157,13 @@ void oracle_append(int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
                    void *k_cache, void *v_cache)
 {
     const int64_t num_slots = (int64_t)num_pages * page_size;
-    for (int32_t t = 0; t < num_tokens; ++t) {
+    int32_t t;
+    /* tokens write distinct slots (a caller mapping two tokens to one slot is
+     * an error on both sides), so the token loop can run on several threads */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (t = 0; t < num_tokens; ++t) {
         if (abort_flags && abort_flags[t])
             continue;
         int64_t slot = slot_mapping[t];
