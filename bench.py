@@ -59,59 +59,88 @@ def dist_info():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    """nvidia-smi clock / throttle samples (every 200 ms), each stamped with the
+    host time it arrived, so the ones inside the timed region can be picked."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.samples = []
 
-    def __enter__(self):
+    def start(self):
+        import threading
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
-                stderr=subprocess.DEVNULL)
-        except (OSError, ValueError):
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
             self.proc = None
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                self.samples.append((time.perf_counter(), line))
+
+        threading.Thread(target=reader, daemon=True).start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < 5.0:   # wait for the first sample
+            time.sleep(0.02)
         return self
 
-    def __exit__(self, *exc):
+    def stop(self):
         if self.proc is not None:
+            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-            self.f.close()
 
-    def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in list(self.samples):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        where = "timed region"
+        if not inside:      # a region shorter than the 200 ms sampling period
+            inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+            where = "within 250 ms of the timed region"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        reasons = sorted({n for r in inside for n, v in zip(self.NAMES, r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
+                "window": where, "reasons": reasons}
+
+
+def aggregate_ranks(step_ms: float, kv_bytes: int, requests: int, device="cpu"):
+    """Whole-job figures over all ranks: the slowest rank's step time, and the
+    bytes / requests every rank processed in it (weak scaling, replicas)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        ms, total_bytes, total_req = step_ms, kv_bytes, requests
+    else:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        n = torch.tensor([kv_bytes, requests], dtype=torch.float64, device=device)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        ms, total_bytes, total_req = float(t.item()), float(n[0].item()), float(n[1].item())
+    return {"ms_per_step": ms, "value_gbs": total_bytes / (ms / 1e3) / 1e9,
+            "tokens_per_s": total_req / (ms / 1e3)}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -257,24 +286,22 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    with sampler:
-        t_wall0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush.zero_()                 # L2 flushed before every timed step
-                step(evs[i])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+    sampler = ClockSampler(local).start()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()                 # L2 flushed before every timed step
+            step(evs[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    t_wall = t_wall1 - t_wall0
+    sampler.stop()
     if world > 1:
         dist.barrier()
     parts = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                       for i in range(args.steps)])          # ms
-    step_ms = float(parts.sum(axis=1).mean())
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    agg = aggregate_ranks(float(parts.sum(axis=1).mean()), kv_bytes, w.batch, device=dev)
+    step_ms = agg["ms_per_step"]
     tag_ms, app_ms, split_ms, comb_ms = (float(x) for x in parts.mean(axis=0))
 
     # ---- end to end: host (pinned) inputs -> device -> step -> host result
@@ -289,7 +316,7 @@ def run_ours(args):
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 200))
     e2e_ms = []
     with torch.cuda.stream(stream):
         for i in range(e2e_steps + 2):
@@ -346,7 +373,7 @@ def run_ours(args):
                      "fp8_attn_speedup": round(bms / (split_ms + comb_ms), 3)}
 
     if rank == 0:
-        value = world * kv_bytes / (step_ms / 1e3) / 1e9
+        value = agg["value_gbs"]
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
@@ -358,7 +385,7 @@ def run_ours(args):
                        "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
                        "l2": "flushed before every timed step (512 MiB write)",
                        "parallelism": f"replicas x{world}"},
-            "tokens_per_s": round(world * w.batch / (step_ms / 1e3), 1),
+            "tokens_per_s": round(agg["tokens_per_s"], 1),
             "hbm_frac_of_measured": round(kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
             "kernel_us": {"tag_check": round(tag_ms * 1e3, 2), "append": round(app_ms * 1e3, 2),
                           "decode_split": round(split_ms * 1e3, 2),
@@ -372,7 +399,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 4 * args.steps,
             "bf16_cache": bf16_line,
-            "clocks": sampler.summary(),
+            "clocks": sampler.summary(t_wall0, t_wall1),
             "wall_s_timed_region": round(t_wall, 3),
             "device_error_bits": dev_err,
         }
@@ -387,8 +414,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="uniform8")
     ap.add_argument("--num-splits", type=int, default=0)
