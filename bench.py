@@ -265,16 +265,11 @@ def run_ours(args):
         dw.append(dw.abort, stream)
         if ev is not None:
             ev[2].record(stream)
-        kvq.kvq_decode_attn_partial(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
-                                    dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out,
-                                    ws, args.num_splits, stream)
+        kvq.kvq_decode_attn(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
+                            dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out, ws,
+                            args.num_splits, stream)
         if ev is not None:
             ev[3].record(stream)
-        kvq.kvq_decode_attn_combine(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
-                                    dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out,
-                                    ws, args.num_splits, stream)
-        if ev is not None:
-            ev[4].record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -282,7 +277,7 @@ def run_ours(args):
             step()
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -298,11 +293,11 @@ def run_ours(args):
     sampler.stop()
     if world > 1:
         dist.barrier()
-    parts = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+    parts = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)]
                       for i in range(args.steps)])          # ms
     agg = aggregate_ranks(float(parts.sum(axis=1).mean()), kv_bytes, w.batch, device=dev)
     step_ms = agg["ms_per_step"]
-    tag_ms, app_ms, split_ms, comb_ms = (float(x) for x in parts.mean(axis=0))
+    tag_ms, app_ms, attn_ms = (float(x) for x in parts.mean(axis=0))
 
     # ---- end to end: host (pinned) inputs -> device -> step -> host result
     host = {
@@ -337,7 +332,7 @@ def run_ours(args):
 
     dev_err = kvq.kvq_device_error()
     peak, peak_kind = measured_peaks()
-    achieved = kv_bytes / (split_ms / 1e3) / 1e9
+    achieved = kv_bytes / (attn_ms / 1e3) / 1e9
     traffic = None
     if os.path.exists(PROFILE_SUMMARY):
         prof = json.load(open(PROFILE_SUMMARY))
@@ -370,7 +365,7 @@ def run_ours(args):
                      "kv_gbs": round(w.kv_bytes(2) / (bms / 1e3) / 1e9, 1),
                      "kv_bytes_per_token_per_layer": w.num_kv_heads * w.head_dim * 2 * 2,
                      "fp8_kv_bytes_per_token_per_layer": w.num_kv_heads * w.head_dim * 2,
-                     "fp8_attn_speedup": round(bms / (split_ms + comb_ms), 3)}
+                     "fp8_attn_speedup": round(bms / attn_ms, 3)}
 
     if rank == 0:
         value = agg["value_gbs"]
@@ -388,8 +383,7 @@ def run_ours(args):
             "tokens_per_s": round(agg["tokens_per_s"], 1),
             "hbm_frac_of_measured": round(kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
             "kernel_us": {"tag_check": round(tag_ms * 1e3, 2), "append": round(app_ms * 1e3, 2),
-                          "decode_split": round(split_ms * 1e3, 2),
-                          "decode_combine": round(comb_ms * 1e3, 2)},
+                          "decode_attn (split + fused combine)": round(attn_ms * 1e3, 2)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": "decode_split_kernel", "peak_kind": peak_kind,
@@ -397,7 +391,7 @@ def run_ours(args):
             "e2e": {"value": round(kv_bytes / (e2e_ms_mean / 1e3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms_mean, 4), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "bf16_cache": bf16_line,
             "clocks": sampler.summary(t_wall0, t_wall1),
             "wall_s_timed_region": round(t_wall, 3),

@@ -63,8 +63,6 @@ _SIGS = {
                         "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
 }
-_SIGS["kvq_decode_attn_partial"] = _SIGS["kvq_decode_attn"]
-_SIGS["kvq_decode_attn_combine"] = _SIGS["kvq_decode_attn"]
 EXPORTED = tuple(_SIGS) + ("kvq_status_string",)
 
 
@@ -197,22 +195,6 @@ def kvq_decode_attn(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, se
     """Paged decode attention into ``out`` (bf16 or fp32 [B][Hq][D])."""
     return _decode("kvq_decode_attn", desc, q, k_cache, v_cache, k_scale, v_scale, block_table,
                    seq_lens, softmax_scale, abort_flags, out, workspace, num_splits, stream)
-
-
-def kvq_decode_attn_partial(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
-                            softmax_scale, abort_flags, out, workspace, num_splits=0, stream=None):
-    """First half of kvq_decode_attn (the split kernel)."""
-    return _decode("kvq_decode_attn_partial", desc, q, k_cache, v_cache, k_scale, v_scale,
-                   block_table, seq_lens, softmax_scale, abort_flags, out, workspace, num_splits,
-                   stream)
-
-
-def kvq_decode_attn_combine(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
-                            softmax_scale, abort_flags, out, workspace, num_splits=0, stream=None):
-    """Second half of kvq_decode_attn (the log-sum-exp combine kernel)."""
-    return _decode("kvq_decode_attn_combine", desc, q, k_cache, v_cache, k_scale, v_scale,
-                   block_table, seq_lens, softmax_scale, abort_flags, out, workspace, num_splits,
-                   stream)
 
 
 def kvq_device_error(clear: bool = False) -> int:

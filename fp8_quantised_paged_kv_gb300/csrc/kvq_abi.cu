@@ -13,10 +13,8 @@ using kvq::kChunkTokens;
 using kvq::kHeadDim;
 
 constexpr int kMaxSplitTokens = 8192;
-constexpr int kMinAutoSplitTokens = 512;
+constexpr int kMinAutoSplitTokens = 256;
 constexpr int kMaxSplitsTotal = 1024;
-constexpr int kCtasPerSm = 2;          // resident CTAs of the persistent split kernel per SM
-constexpr int kUnitsPerCta = 8;        // the automatic split size aims at this many units per CTA
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -57,9 +55,40 @@ kvq_status check_desc(const kvq_cache_desc *d)
 }
 
 struct Plan {
-    int32_t split_tokens, max_splits, grid;
-    size_t lse_bytes, o_bytes;
+    int32_t split_tokens, max_splits;
+    size_t counter_bytes, lse_bytes, o_bytes;
 };
+
+// Automatic split count per (request, KV head).  Large jobs use the largest
+// split (8,192 tokens): there are many waves of CTAs anyway.  Small jobs pick
+// the count whose CTAs best fill whole waves of the resident CTA slots (SMs x
+// CTAs per SM), preferring fewer waves, with splits of at least 256 tokens.
+int64_t auto_splits(int64_t pairs, int64_t max_ctx, int64_t slots)
+{
+    const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
+    if (pairs * big >= 4 * slots)
+        return big;
+    int64_t most = max_ctx / kMinAutoSplitTokens;
+    if (most < 1)
+        most = 1;
+    if (most > kMaxSplitsTotal)
+        most = kMaxSplitsTotal;
+    int64_t best = 1;
+    double best_score = -1.0;
+    for (int64_t n = 1; n <= most; ++n) {
+        const int64_t ctas = pairs * n;
+        const int64_t waves = (ctas + slots - 1) / slots;
+        if (waves > 4)
+            break;
+        const double fill = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+        const double score = fill - 0.1 * static_cast<double>(waves);
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = n;
+        }
+    }
+    return best;
+}
 
 kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads,
                      int32_t max_pages, int32_t num_splits, Plan *p)
@@ -69,7 +98,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         return st;
     if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0)
         return KVQ_ERR_INVALID_ARG;
-    if (batch > kvq::decode_max_batch())
+    if (batch > 65535)
         return KVQ_ERR_UNSUPPORTED;
     if (num_q_heads % d->num_kv_heads != 0)
         return KVQ_ERR_INVALID_ARG;
@@ -82,12 +111,8 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (num_splits > 0) {
         want = num_splits;
     } else {
-        const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kUnitsPerCta;
-        const int64_t work = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads * max_ctx;
-        int64_t per = (work + target - 1) / target;
-        if (per < kMinAutoSplitTokens)
-            per = kMinAutoSplitTokens;
-        want = (max_ctx + per - 1) / per;
+        const int64_t slots = static_cast<int64_t>(sm_count()) * kvq::decode_ctas_per_sm();
+        want = auto_splits(static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads, max_ctx, slots);
     }
     if (want < 1)
         want = 1;
@@ -100,9 +125,9 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         return KVQ_ERR_UNSUPPORTED;
     p->split_tokens = static_cast<int32_t>(split);
     p->max_splits = static_cast<int32_t>(splits);
-    const int64_t units = static_cast<int64_t>(batch) * d->num_kv_heads * splits;
-    const int64_t slots = static_cast<int64_t>(sm_count()) * kCtasPerSm;
-    p->grid = static_cast<int32_t>(units < slots ? (units > 0 ? units : 1) : slots);
+    p->counter_bytes = (static_cast<size_t>(batch) * d->num_kv_heads * 4 + 255) / 256 * 256;
+    if (p->counter_bytes == 0)
+        p->counter_bytes = 256;
     if (splits > 1) {
         const size_t n = static_cast<size_t>(batch) * num_q_heads * splits;
         p->lse_bytes = (n * sizeof(float) + 255) / 256 * 256;
@@ -189,7 +214,7 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     }
     if (batch > 65535)
         return KVQ_ERR_UNSUPPORTED;
-    const size_t need = kvq::kCounterBytes + call->plan.lse_bytes + call->plan.o_bytes;
+    const size_t need = call->plan.counter_bytes + call->plan.lse_bytes + call->plan.o_bytes;
     if (workspace == nullptr || workspace_bytes < need)
         return KVQ_ERR_WORKSPACE;
     if (!aligned16(workspace))
@@ -204,9 +229,9 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     a.out = out;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.counters = reinterpret_cast<unsigned int *>(ws);
-    a.ws_lse = call->plan.lse_bytes ? reinterpret_cast<float *>(ws + kvq::kCounterBytes) : nullptr;
+    a.ws_lse = call->plan.lse_bytes ? reinterpret_cast<float *>(ws + call->plan.counter_bytes) : nullptr;
     a.ws_o = call->plan.o_bytes
-                 ? reinterpret_cast<float *>(ws + kvq::kCounterBytes + call->plan.lse_bytes)
+                 ? reinterpret_cast<float *>(ws + call->plan.counter_bytes + call->plan.lse_bytes)
                  : nullptr;
     a.batch = batch;
     a.num_q_heads = num_q_heads;
@@ -312,51 +337,8 @@ kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t nu
     if (max_splits)
         *max_splits = p.max_splits;
     if (workspace_bytes)
-        *workspace_bytes = kvq::kCounterBytes + p.lse_bytes + p.o_bytes;
+        *workspace_bytes = p.counter_bytes + p.lse_bytes + p.o_bytes;
     return KVQ_OK;
-}
-
-kvq_status kvq_decode_attn_partial(const kvq_cache_desc *desc, const void *q, int32_t batch,
-                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
-                                   const float *k_scale, const float *v_scale,
-                                   const int32_t *block_table, int32_t max_pages_per_seq,
-                                   const int32_t *seq_lens, float softmax_scale,
-                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
-                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
-                                   kvq_stream_t stream)
-{
-    DecodeCall call;
-    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
-                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
-                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
-                                   num_splits, &call);
-    if (st != KVQ_OK || batch == 0)
-        return st;
-    CUtensorMap km, vm;
-    if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
-        return KVQ_ERR_CUDA;
-    return to_status(kvq::launch_decode_partial(call.args, km, vm,
-                                                reinterpret_cast<cudaStream_t>(stream),
-                                                call.plan.grid));
-}
-
-kvq_status kvq_decode_attn_combine(const kvq_cache_desc *desc, const void *q, int32_t batch,
-                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
-                                   const float *k_scale, const float *v_scale,
-                                   const int32_t *block_table, int32_t max_pages_per_seq,
-                                   const int32_t *seq_lens, float softmax_scale,
-                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
-                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
-                                   kvq_stream_t stream)
-{
-    DecodeCall call;
-    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
-                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
-                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
-                                   num_splits, &call);
-    if (st != KVQ_OK || batch == 0)
-        return st;
-    return to_status(kvq::launch_decode_combine(call.args, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t batch,
@@ -377,11 +359,7 @@ kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t ba
     CUtensorMap km, vm;
     if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
         return KVQ_ERR_CUDA;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = kvq::launch_decode_partial(call.args, km, vm, s, call.plan.grid);
-    if (e != cudaSuccess)
-        return KVQ_ERR_CUDA;
-    return to_status(kvq::launch_decode_combine(call.args, s));
+    return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_device_error(uint32_t *bits, int32_t clear)

@@ -36,11 +36,11 @@ struct TagCheckArgs {
 cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream);
 
 // Workspace layout (bytes from the workspace base):
-//   [0, 256)                 uint32 counters[2]: next work unit, finished CTAs
-//                            (zero before the first call; every call leaves them zero)
-//   [256, +lse_bytes)        fp32 lse[B][Hq][S]  (log2 domain, NaN = invalid split)
-//   [.., +o_bytes)           fp32 o[B][Hq][S][D]  (each split's normalised output)
-constexpr size_t kCounterBytes = 256;
+//   [0, counter_bytes)       uint32 arrivals[B][Hkv]: splits of each (request, KV
+//                            head) that have published; zero before the first
+//                            call, and every call leaves them zero
+//   [counter_bytes, +lse)    fp32 lse[B][Hq][S]  (log2 domain, NaN = invalid split)
+//   [.., +o)                 fp32 o[B][Hq][S][D]  (each split's normalised output)
 struct DecodeArgs {
     const void *q;                   // bf16 [B][Hq][D]
     const float *k_scale, *v_scale;  // [Hkv] (unused for bf16 cache)
@@ -57,12 +57,12 @@ struct DecodeArgs {
     bool out_fp32, bf16_cache;
 };
 
-// Split kernel + combine kernel.  The tensor maps describe the K and V
-// caches as 2-D [rows][128 bytes] tensors with 128-byte swizzle.
-cudaError_t launch_decode_partial(const DecodeArgs &a, const CUtensorMap &k_map,
-                                  const CUtensorMap &v_map, cudaStream_t stream, int grid);
-int decode_max_batch();
-cudaError_t launch_decode_combine(const DecodeArgs &a, cudaStream_t stream);
+// Split kernel with the combine fused into its epilogue.  The tensor maps
+// describe the K and V caches as 2-D [rows][128 bytes] tensors with 128-byte
+// swizzle.
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                          cudaStream_t stream);
+int decode_ctas_per_sm();
 
 // Box height (in 128-byte rows) of one bulk copy for a page size.
 inline int tma_box_rows(int page_size, bool bf16_cache)

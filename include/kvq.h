@@ -44,7 +44,7 @@
  *     elements.  A token at logical position j of request r lives in page
  *     block_table[r][j / page_size], slot j % page_size.
  *   - Supported: head_dim 128; page_size 16, 32, 64 or 128; query heads per
- *     KV head (g = num_q_heads / num_kv_heads) 1 to 8; up to 1024 requests
+ *     KV head (g = num_q_heads / num_kv_heads) 1 to 8; up to 65535 requests
  *     per decode call.  Others return KVQ_ERR_UNSUPPORTED.
  */
 #ifndef KVQ_H
@@ -142,13 +142,16 @@ KVQ_API kvq_status kvq_tag_check(const int32_t *block_table, const uint32_t *exp
  * context and how many workspace bytes it needs.
  *
  *   num_splits     requested splits per (request, KV head); 0 = automatic
- *                  (sized from the device's SM count and the batch).
+ *                  (sized from the device's SM count and the batch).  A split
+ *                  never exceeds 8,192 tokens, so long contexts get at least
+ *                  ceil(context / 8192) splits.
  *   *split_tokens  OUT: tokens per split (a multiple of 32).
  *   *max_splits    OUT: splits of the longest possible request,
  *                  ceil(max_pages_per_seq * page_size / *split_tokens).
- *   *workspace_bytes OUT: bytes of workspace kvq_decode_attn needs: a
- *                  256-byte scheduling header plus, when a request can span
- *                  more than one split, the per-split partial results.
+ *   *workspace_bytes OUT: bytes of workspace kvq_decode_attn needs: the
+ *                  arrival counters (4 bytes per request and KV head, padded
+ *                  to 256) plus, when a request can span more than one
+ *                  split, the per-split partial results.
  * Any OUT pointer may be NULL.
  */
 KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
@@ -177,15 +180,16 @@ KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, in
  *                  aborted, empty (seq_len <= 0), longer than their table row
  *                  or that name a page outside [0, num_pages) get zeros.
  *   workspace      device scratch of at least the kvq_decode_plan size for
- *                  the same arguments.  Its first 256 bytes are the work
- *                  counters of the persistent split kernel: they must be zero
- *                  before the first call that uses the buffer, and every call
- *                  leaves them zero again.  The rest holds the per-split
- *                  partial results between the split and combine kernels of
- *                  one call.  Two calls in flight at once must not share it.
+ *                  the same arguments.  It starts with one uint32 arrival
+ *                  counter per (request, KV head), padded to 256 bytes: they
+ *                  must be zero before the first call that uses the buffer,
+ *                  and every call leaves them zero again.  The rest holds the
+ *                  per-split partial results (lse, o) of one call.  Two calls
+ *                  in flight at once must not share a workspace.
  *   num_splits     as in kvq_decode_plan.
- * Launches the split kernel and, when some request spans more than one
- * split, the log-sum-exp combine kernel.
+ * One kernel launch: every (split, KV head, request) is one CTA; the last
+ * split of a (request, KV head) to finish merges the splits' partials by
+ * their log-sum-exp weights (the combine) before it exits.
  */
 KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t batch,
                            int32_t num_q_heads, const void *k_cache, const void *v_cache,
@@ -195,30 +199,6 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, in
                            const uint8_t *abort_flags, void *out, int32_t out_dtype,
                            void *workspace, size_t workspace_bytes, int32_t num_splits,
                            kvq_stream_t stream);
-
-/*
- * The two halves of kvq_decode_attn, for callers that want to place other
- * work (or timing events) between them.  Same arguments; call partial, then
- * combine, on the same stream with the same workspace.  partial writes the
- * final output of every request that fits in one split (and the zeros of
- * aborted, empty or invalid ones); combine merges the rest.
- */
-KVQ_API kvq_status kvq_decode_attn_partial(const kvq_cache_desc *desc, const void *q, int32_t batch,
-                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
-                                   const float *k_scale, const float *v_scale,
-                                   const int32_t *block_table, int32_t max_pages_per_seq,
-                                   const int32_t *seq_lens, float softmax_scale,
-                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
-                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
-                                   kvq_stream_t stream);
-KVQ_API kvq_status kvq_decode_attn_combine(const kvq_cache_desc *desc, const void *q, int32_t batch,
-                                   int32_t num_q_heads, const void *k_cache, const void *v_cache,
-                                   const float *k_scale, const float *v_scale,
-                                   const int32_t *block_table, int32_t max_pages_per_seq,
-                                   const int32_t *seq_lens, float softmax_scale,
-                                   const uint8_t *abort_flags, void *out, int32_t out_dtype,
-                                   void *workspace, size_t workspace_bytes, int32_t num_splits,
-                                   kvq_stream_t stream);
 
 /*
  * kvq_device_error -- HOST call, synchronous: reads (into *bits, host

@@ -50,7 +50,7 @@ def test_plan_splits_cover_the_context():
                 ctx = maxp * ps
                 assert st % 32 == 0 and st % min(ps, 32) == 0 and st % ps == 0 and st <= 8192
                 assert ms == -(-ctx // st)
-                assert (ws == 256) == (ms == 1)      # the 256-byte counter header is always there
+                assert (ws == 256) == (ms == 1)      # the arrival counters (8 x 8 x 4 B, padded) are always there
                 if splits:
                     assert ms <= max(splits, -(-ctx // 8192))
 
@@ -103,10 +103,20 @@ def test_workspace_too_small_is_reported():
     assert st == 3
     st = lib.kvq_decode_attn(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p,
                              ctypes.c_float(0.1), None, p, 0, None, 1 << 30, 0, None)
-    assert st == 3                      # the counter header is always needed
+    assert st == 3                      # the arrival counters are always needed
+
+
+def test_auto_split_fills_the_resident_slots():
+    # 8 requests x 8 KV heads at 8,208 tokens: 7 splits fill 448 of the 456
+    # resident CTA slots of a 152-SM part in one wave; a host without a GPU
+    # plans for 148 SMs (444 slots: 6 splits = 384 CTAs, or 7 = 448 in 2 waves)
+    st, ms, _ = _plan(ps=16, hkv=8, B=8, hq=64, maxp=513)
+    assert ms in (6, 7)
+    st, ms, _ = _plan(ps=64, hkv=8, B=4, hq=16, maxp=16384)     # long contexts
+    assert st == 8192 and ms == 128
 
 
 def test_batch_limit():
     with pytest.raises(kvq.KvqError) as e:
-        _plan(B=1025)
+        _plan(B=65536)
     assert e.value.status == 2
