@@ -62,6 +62,8 @@ _SIGS = {
     "kvq_decode_attn": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
                         "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
+    "kvq_decode_attn_static_ws": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p",
+                                  "f32", "p", "p", "i32", "i32", "p"],
 }
 EXPORTED = tuple(_SIGS) + ("kvq_status_string",)
 

@@ -201,6 +201,39 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, in
                            kvq_stream_t stream);
 
 /*
+ * kvq_decode_attn_static_ws -- kvq_decode_attn for callers that cannot
+ * allocate device memory while they decode (an engine that has already
+ * handed all of its device memory to its own pool, or C code that holds no
+ * allocator).  The source pages have no counterpart to this entry point.
+ *
+ * Same arguments and results as kvq_decode_attn, without the workspace: the
+ * scratch is one array of KVQ_STATIC_WS_BYTES (16 MiB) compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing.
+ *   - A call whose kvq_decode_plan workspace size exceeds KVQ_STATIC_WS_BYTES
+ *     returns KVQ_ERR_WORKSPACE before touching the GPU; pass a smaller
+ *     num_splits, or use kvq_decode_attn with a workspace of your own.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (once per device); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     each call clears the part that must start at zero (the arrival
+ *     counters) on its stream before the kernel runs.  Calls that overlap on
+ *     the GPU (other streams, other threads) race on the array: serialise
+ *     them.
+ */
+#define KVQ_STATIC_WS_BYTES (16u << 20)
+KVQ_API kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc *desc, const void *q,
+                                             int32_t batch, int32_t num_q_heads,
+                                             const void *k_cache, const void *v_cache,
+                                             const float *k_scale, const float *v_scale,
+                                             const int32_t *block_table,
+                                             int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                             float softmax_scale, const uint8_t *abort_flags,
+                                             void *out, int32_t out_dtype, int32_t num_splits,
+                                             kvq_stream_t stream);
+
+/*
  * kvq_device_error -- HOST call, synchronous: reads (into *bits, host
  * memory) and, if `clear` is non-zero, resets the sticky device error word
  * of the current device.  Bit 0: a bulk-copy wait in the decode split kernel
