@@ -32,25 +32,25 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a)
     const bool is_v = rem >= a.num_kv_heads;
     const int h = is_v ? rem - a.num_kv_heads : rem;
 
-    if (a.abort_flags != nullptr && a.abort_flags[t] != 0)
-        return;
-    const int64_t slot = a.slot_mapping[t];
-    if (slot < 0 || slot >= a.num_slots)
+    // every load is issued before the first decision, so the kernel waits on
+    // one round trip to memory, not a chain of them
+    const uint16_t *src = static_cast<const uint16_t *>(is_v ? a.v_new : a.k_new) +
+                          (t * a.num_kv_heads + h) * kHeadDim + part * 8;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src));
+    const int64_t slot = __ldg(a.slot_mapping + t);
+    const bool aborted = a.abort_flags != nullptr && __ldg(a.abort_flags + t) != 0;
+    const float scale = kBf16Cache ? 1.f : __ldg((is_v ? a.v_scale : a.k_scale) + h);
+    if (aborted || slot < 0 || slot >= a.num_slots)
         return;
     const int64_t page = slot / a.page_size;
     const int64_t off = slot % a.page_size;
     const int64_t dst_row = (page * a.num_kv_heads + h) * a.page_size + off;
-
-    const uint16_t *src = static_cast<const uint16_t *>(is_v ? a.v_new : a.k_new) +
-                          (t * a.num_kv_heads + h) * kHeadDim + part * 8;
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src));
 
     if constexpr (kBf16Cache) {
         uint16_t *dst = static_cast<uint16_t *>(is_v ? a.v_cache : a.k_cache) +
                         dst_row * kHeadDim + part * 8;
         *reinterpret_cast<uint4 *>(dst) = x;
     } else {
-        const float scale = (is_v ? a.v_scale : a.k_scale)[h];
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t packed[2];
 #pragma unroll

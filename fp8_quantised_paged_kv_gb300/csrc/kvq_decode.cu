@@ -93,42 +93,15 @@ __device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool 
 }
 
 
-// Shared-memory offset (in floats) of the combine scratch: past the warps'
-// merge area, inside the ring (which is idle by then).
-constexpr int kScratchOffset = 8192;
-
-__device__ __forceinline__ float block_max(float v, float *red)
-{
-    for (int off = 16; off > 0; off >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
-    if (threadIdx.x % 32 == 0)
-        red[threadIdx.x / 32] = v;
-    __syncthreads();
-    float r = red[0];
-    for (int w = 1; w < kWarps; ++w)
-        r = fmaxf(r, red[w]);
-    __syncthreads();
-    return r;
-}
-
-__device__ __forceinline__ float block_sum(float v, float *red)
-{
-    for (int off = 16; off > 0; off >>= 1)
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    if (threadIdx.x % 32 == 0)
-        red[threadIdx.x / 32] = v;
-    __syncthreads();
-    float r = 0.f;
-    for (int w = 0; w < kWarps; ++w)
-        r += red[w];
-    __syncthreads();
-    return r;
-}
+// Shared-memory offset (in floats) of the combine scratch: just past the
+// warps' merge area, inside the ring (idle by then).
+constexpr int kScratchOffset = (kWarps * kMaxGroup * kHeadDim + 2 * kWarps * kMaxGroup + 3) / 4 * 4;
 
 // Count this split's arrival for (request b, KV head kvh).  The last split
 // to arrive merges the partials of all nsplit splits of the group:
 //   M = max_s lse_s,  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
-// writes the output (zeros if any split was invalid) and resets the counter.
+// for every query head of the group at once, writes the output (zeros for
+// a head if any split was invalid) and resets the counter.
 __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsplit, float *scratch)
 {
     __shared__ int s_last;
@@ -141,43 +114,56 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
     if (!s_last)
         return;
     __threadfence();
-    float *s_w = scratch;                    // [nsplit] weights
-    float *red = scratch + kMaxSplits;       // [kWarps]
-    for (int h = 0; h < a.group; ++h) {
-        const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + kvh * a.group + h;
-        const float *lse = a.ws_lse + bh * a.max_splits;
-        float mloc = -INFINITY;
-        bool badl = false;
-        for (int s = threadIdx.x; s < nsplit; s += kThreads) {
-            const float v = __ldcg(lse + s);
-            badl |= v != v;
-            s_w[s] = v;
-            mloc = fmaxf(mloc, v);
+    const int g = a.group, n = nsplit;
+    const int64_t bh0 = static_cast<int64_t>(b) * a.num_q_heads + kvh * g;
+    float *s_tot = scratch;                  // [8] sum of weights (0: drop the head)
+    float *s_w = scratch + kMaxGroup;        // [g][n]: lse, then weights
+    for (int i = threadIdx.x; i < g * n; i += kThreads)
+        s_w[i] = __ldcg(a.ws_lse + (bh0 + i / n) * a.max_splits + i % n);
+    __syncthreads();
+    // one warp per head: max, validity, weights, their sum
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int h = warp; h < g; h += kWarps) {
+        float *w = s_w + h * n;
+        float m = -INFINITY;
+        bool bad = false;
+        for (int s = lane; s < n; s += 32) {
+            bad |= w[s] != w[s];
+            m = fmaxf(m, w[s]);
         }
-        const bool bad = __syncthreads_or(badl);
-        const float mmax = block_max(mloc, red);
-        float wloc = 0.f;
-        for (int s = threadIdx.x; s < nsplit; s += kThreads) {
-            const float wgt = bad ? 0.f : fast_exp2(s_w[s] - mmax);
-            s_w[s] = wgt;
-            wloc += wgt;
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        for (int off = 16; off > 0; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        float sum = 0.f;
+        for (int s = lane; s < n; s += 32) {
+            const float e = bad ? 0.f : fast_exp2(w[s] - m);
+            w[s] = e;
+            sum += e;
         }
-        const float total = block_sum(wloc, red);
-        const float *ob = a.ws_o + bh * a.max_splits * kHeadDim;
-        for (int d = threadIdx.x; d < kHeadDim; d += kThreads) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            int s = 0;
-            for (; s + 4 <= nsplit; s += 4) {
+        for (int off = 16; off > 0; off >>= 1)
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        if (lane == 0)
+            s_tot[h] = bad ? 0.f : sum;
+    }
+    __syncthreads();
+    // thread d: every head of the group, all splits, loads independent across heads
+    for (int d = threadIdx.x; d < kHeadDim; d += kThreads) {
+        float acc[kMaxGroup];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[j] += s_w[s + j] * __ldcg(ob + static_cast<int64_t>(s + j) * kHeadDim + d);
-            }
-            for (; s < nsplit; ++s)
-                acc[0] += s_w[s] * __ldcg(ob + static_cast<int64_t>(s) * kHeadDim + d);
-            const float v = bad ? 0.f : (acc[0] + acc[1] + acc[2] + acc[3]) / total;
-            store_out(a.out, bh * kHeadDim + d, v, a.out_fp32);
+        for (int h = 0; h < kMaxGroup; ++h)
+            acc[h] = 0.f;
+        for (int s = 0; s < n; ++s) {
+#pragma unroll
+            for (int h = 0; h < kMaxGroup; ++h)
+                if (h < g)
+                    acc[h] += s_w[h * n + s] *
+                              __ldcg(a.ws_o + ((bh0 + h) * a.max_splits + s) * kHeadDim + d);
         }
-        __syncthreads();                     // s_w is reused by the next head
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h)
+            if (h < g)
+                store_out(a.out, (bh0 + h) * kHeadDim + d, s_tot[h] > 0.f ? acc[h] / s_tot[h] : 0.f,
+                          a.out_fp32);
     }
     if (threadIdx.x == 0)
         *counter = 0;                        // ready for the next call
@@ -220,6 +206,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int g = a.group, ps = a.page_size;
     const int hq0 = kvh * g;                               // first query head of the group
 
+    // The block-table entries this split can use depend only on the split
+    // index, so they are loaded together with the request's length.
+    const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
+    const int span_left = a.max_pages_per_seq - first_page;
+    const int span = a.split_tokens / ps < span_left ? a.split_tokens / ps : span_left;
+    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
+    constexpr int kIdsPerThread = (kMaxPageList + kThreads - 1) / kThreads;
+    int32_t ids[kIdsPerThread];
+#pragma unroll
+    for (int k = 0; k < kIdsPerThread; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        ids[k] = i < span ? __ldg(bt + i) : -1;
+    }
     const int64_t len = a.seq_lens[b];
     const bool aborted = a.abort_flags != nullptr && a.abort_flags[b] != 0;
     const int64_t cap = static_cast<int64_t>(a.max_pages_per_seq) * ps;
@@ -238,14 +237,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int64_t t0 = static_cast<int64_t>(split) * a.split_tokens;
     const int64_t t1 = min(len, t0 + a.split_tokens);
     // page ids of this split (t0 is a multiple of the page size)
-    const int first_page = static_cast<int>(t0 / ps);
     const int n_pages = static_cast<int>((t1 - 1) / ps) - first_page + 1;
-    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
     bool bad = false;
-    for (int i = threadIdx.x; i < n_pages; i += kThreads) {
-        const int32_t p = bt[i];
-        bad |= (p < 0 || p >= a.num_pages);
-        page_list[i] = p;
+#pragma unroll
+    for (int k = 0; k < kIdsPerThread; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        if (i < n_pages) {
+            bad |= (ids[k] < 0 || ids[k] >= a.num_pages);
+            page_list[i] = ids[k];
+        }
     }
     if (threadIdx.x == 0) {
         s_failed = 0;

@@ -8,17 +8,18 @@
 // (blog post "Smaller, faster, safer", page-2 mirror section "KV Cache
 // 完整性检查"; page-3 mirror section "一个不能出错的共享缓存").
 //
-// One CTA per request: its threads take the ceil(L / page_size) entries the
-// request uses in one strided pass (coalesced block-table and expected-tag
-// loads, one gather of the live tag each), OR-reduce with __syncthreads_or,
-// and thread 0 writes the flag (0 or 1).  A 513-page request costs one round
-// of dependent loads instead of 17 rounds on a single warp.
+// One CTA per request: its 256 threads take the ceil(L / page_size) entries
+// the request uses, 1,024 per pass, issuing every block-table and
+// expected-tag load of the pass before the live-tag gathers, so a pass costs
+// two rounds of dependent loads; OR-reduce with __syncthreads_or; thread 0
+// writes the flag (0 or 1).
 #include "kvq_internal.h"
 
 namespace kvq {
 namespace {
 
-constexpr int kTagThreads = 128;
+constexpr int kTagThreads = 256;
+constexpr int kTagUnroll = 4;          // entries per thread per pass: all loads issued before any use
 
 __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
 {
@@ -32,11 +33,26 @@ __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
     }
     const int32_t *bt = a.block_table + r * a.max_pages_per_seq;
     const uint32_t *exp = a.expected_tags + r * a.max_pages_per_seq;
-    for (int64_t i = threadIdx.x; i < used; i += kTagThreads) {
-        const int32_t p = __ldg(bt + i);
-        const uint32_t want = __ldg(exp + i);
-        if (p < 0 || p >= a.num_pages || __ldg(a.page_tags + p) != want)
-            bad = true;
+    for (int64_t base = 0; base < used; base += kTagThreads * kTagUnroll) {
+        int32_t p[kTagUnroll];
+        uint32_t want[kTagUnroll], live[kTagUnroll];
+#pragma unroll
+        for (int k = 0; k < kTagUnroll; ++k) {
+            const int64_t i = base + k * kTagThreads + threadIdx.x;
+            p[k] = i < used ? __ldg(bt + i) : 0;
+            want[k] = i < used ? __ldg(exp + i) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kTagUnroll; ++k) {
+            const bool in_range = p[k] >= 0 && p[k] < a.num_pages;
+            live[k] = in_range ? __ldg(a.page_tags + p[k]) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kTagUnroll; ++k) {
+            const int64_t i = base + k * kTagThreads + threadIdx.x;
+            if (i < used && (p[k] < 0 || p[k] >= a.num_pages || live[k] != want[k]))
+                bad = true;
+        }
     }
     bad = __syncthreads_or(bad);
     if (threadIdx.x == 0)
