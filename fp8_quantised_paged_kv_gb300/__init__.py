@@ -62,6 +62,8 @@ _SIGS = {
     "kvq_decode_attn": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
                         "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
+    "kvq_tag_check_append": ["desc", "p", "p", "p", "i32", "i32", "p", "p", "p", "p", "p", "p",
+                             "p", "p", "p", "p"],
     "kvq_decode_attn_static_ws": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p",
                                   "f32", "p", "p", "i32", "i32", "p"],
 }
@@ -151,6 +153,30 @@ def kvq_tag_check(block_table, expected_tags, seq_lens, page_size: int, page_tag
                               page_size, _ptr(page_tags), page_tags.shape[0], _ptr(abort_flags),
                               _stream(stream))
     _check("kvq_tag_check", st)
+
+
+def kvq_tag_check_append(desc: CacheDesc, block_table, expected_tags, seq_lens, page_tags,
+                         k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache,
+                         abort_flags, stream=None):
+    """Tag check of every request, then the append of token r for request r
+    unless it was aborted -- kvq_tag_check + kvq_append in one launch."""
+    import torch
+    B, maxp = block_table.shape
+    _expect(block_table, torch.int32, None, "block_table")
+    if expected_tags.element_size() != 4 or tuple(expected_tags.shape) != (B, maxp):
+        raise ValueError("expected_tags: expected 32-bit tags [B][max_pages]")
+    if page_tags.element_size() != 4 or page_tags.dim() != 1:
+        raise ValueError("page_tags: expected 32-bit tags [num_pages]")
+    _expect(seq_lens, torch.int32, (B,), "seq_lens")
+    _expect(abort_flags, torch.uint8, (B,), "abort_flags")
+    _expect(k_new, torch.bfloat16, (B, desc.num_kv_heads, desc.head_dim), "k_new")
+    _expect(v_new, torch.bfloat16, (B, desc.num_kv_heads, desc.head_dim), "v_new")
+    _expect(slot_mapping, torch.int64, (B,), "slot_mapping")
+    st = load().kvq_tag_check_append(
+        ctypes.byref(desc.c()), _ptr(block_table), _ptr(expected_tags), _ptr(seq_lens), B, maxp,
+        _ptr(page_tags), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_scale),
+        _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), _ptr(abort_flags), _stream(stream))
+    _check("kvq_tag_check_append", st)
 
 
 def kvq_decode_plan(desc: CacheDesc, batch: int, num_q_heads: int, max_pages_per_seq: int,

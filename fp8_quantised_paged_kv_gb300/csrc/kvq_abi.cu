@@ -324,6 +324,58 @@ kvq_status kvq_tag_check(const int32_t *block_table, const uint32_t *expected_ta
     return to_status(kvq::launch_tag_check(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_tag_check_append(const kvq_cache_desc *desc, const int32_t *block_table,
+                                const uint32_t *expected_tags, const int32_t *seq_lens,
+                                int32_t batch, int32_t max_pages_per_seq,
+                                const uint32_t *page_tags, const void *k_new, const void *v_new,
+                                const int64_t *slot_mapping, const float *k_scale,
+                                const float *v_scale, void *k_cache, void *v_cache,
+                                uint8_t *abort_flags, kvq_stream_t stream)
+{
+    kvq_status st = check_desc(desc);
+    if (st != KVQ_OK)
+        return st;
+    if (batch < 0 || max_pages_per_seq <= 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (batch == 0)
+        return KVQ_OK;
+    const bool bf16 = desc->cache_dtype == KVQ_CACHE_BF16;
+    if (!block_table || !expected_tags || !seq_lens || !page_tags || !abort_flags || !k_new ||
+        !v_new || !slot_mapping || !k_cache || !v_cache)
+        return KVQ_ERR_INVALID_ARG;
+    if (!bf16 && (!k_scale || !v_scale))
+        return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return KVQ_ERR_INVALID_ARG;
+    if (desc->num_kv_heads > 64)
+        return KVQ_ERR_UNSUPPORTED;
+    kvq::TagCheckArgs t;
+    t.block_table = block_table;
+    t.expected_tags = expected_tags;
+    t.seq_lens = seq_lens;
+    t.page_tags = page_tags;
+    t.abort_flags = abort_flags;
+    t.batch = batch;
+    t.max_pages_per_seq = max_pages_per_seq;
+    t.page_size = desc->page_size;
+    t.num_pages = desc->num_pages;
+    kvq::AppendArgs a;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slot_mapping = slot_mapping;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.abort_flags = nullptr;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_tokens = batch;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.page_size = desc->page_size;
+    a.num_slots = static_cast<int64_t>(desc->num_pages) * desc->page_size;
+    a.bf16_cache = bf16;
+    return to_status(kvq::launch_tag_check_append(t, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
                            int32_t max_pages_per_seq, int32_t num_splits, int32_t *split_tokens,
                            int32_t *max_splits, size_t *workspace_bytes)

@@ -9,13 +9,11 @@
 // One row = one (token, K|V, KV head) vector of 128 elements; 16 threads per
 // row, each loading 16 bytes (8 bf16) and storing 8 bytes (8 codes), so both
 // the bf16 source and the paged destination are accessed fully coalesced.
-#include "kvq_internal.h"
-#include "kvq_ptx.cuh"
+#include "kvq_rowops.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int kThreadsPerRow = kHeadDim / 8;   // 16
 constexpr int kAppendThreads = 256;
 
 template <bool kBf16Cache>
@@ -46,25 +44,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a)
     const int64_t off = slot % a.page_size;
     const int64_t dst_row = (page * a.num_kv_heads + h) * a.page_size + off;
 
-    if constexpr (kBf16Cache) {
-        uint16_t *dst = static_cast<uint16_t *>(is_v ? a.v_cache : a.k_cache) +
-                        dst_row * kHeadDim + part * 8;
-        *reinterpret_cast<uint4 *>(dst) = x;
-    } else {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t packed[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float2 p0 = bf16x2_to_f32x2(w[2 * i]);
-            const float2 p1 = bf16x2_to_f32x2(w[2 * i + 1]);
-            const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(p0.x, scale), __fdiv_rn(p0.y, scale));
-            const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(p1.x, scale), __fdiv_rn(p1.y, scale));
-            packed[i] = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
-        }
-        uint8_t *dst = static_cast<uint8_t *>(is_v ? a.v_cache : a.k_cache) +
-                       dst_row * kHeadDim + part * 8;
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-    }
+    void *cache = is_v ? a.v_cache : a.k_cache;
+    void *dst = kBf16Cache ? static_cast<void *>(static_cast<uint16_t *>(cache) + dst_row * kHeadDim)
+                           : static_cast<void *>(static_cast<uint8_t *>(cache) + dst_row * kHeadDim);
+    store_row_part<kBf16Cache>(dst, part, x, scale);
 }
 
 } // namespace

@@ -95,7 +95,8 @@ __device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool 
 
 // Shared-memory offset (in floats) of the combine scratch: just past the
 // warps' merge area, inside the ring (idle by then).
-constexpr int kScratchOffset = (kWarps * kMaxGroup * kHeadDim + 2 * kWarps * kMaxGroup + 3) / 4 * 4;
+constexpr int kScratchOffset =
+    (kWarps * kMaxGroup * kHeadDim + 3 * kWarps * kMaxGroup + 2 * kMaxGroup + 3) / 4 * 4;
 
 // Count this split's arrival for (request b, KV head kvh).  The last split
 // to arrive merges the partials of all nsplit splits of the group:
@@ -152,12 +153,23 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
 #pragma unroll
         for (int h = 0; h < kMaxGroup; ++h)
             acc[h] = 0.f;
-        for (int s = 0; s < n; ++s) {
+        // four splits per round: all of the round's loads are issued before
+        // any is used, so a round costs one trip to L2
+        for (int s0 = 0; s0 < n; s0 += 4) {
+            float v[4][kMaxGroup];
 #pragma unroll
-            for (int h = 0; h < kMaxGroup; ++h)
-                if (h < g)
-                    acc[h] += s_w[h * n + s] *
-                              __ldcg(a.ws_o + ((bh0 + h) * a.max_splits + s) * kHeadDim + d);
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int h = 0; h < kMaxGroup; ++h)
+                    v[j][h] = (h < g && s0 + j < n)
+                                  ? __ldcg(a.ws_o + ((bh0 + h) * a.max_splits + s0 + j) * kHeadDim + d)
+                                  : 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int h = 0; h < kMaxGroup; ++h)
+                    if (h < g && s0 + j < n)
+                        acc[h] += s_w[h * n + s0 + j] * v[j][h];
         }
 #pragma unroll
         for (int h = 0; h < kMaxGroup; ++h)
@@ -561,28 +573,41 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     __syncthreads();
 
-    for (int d = threadIdx.x; d < kHeadDim; d += kThreads)
-    for (int h = 0; h < g; ++h) {
+    // per-head merge factors of the four warps, computed once (thread h)
+    float *sm_f = sm_l + kWarps * kMaxGroup;                          // [8][kWarps] weights
+    float *sm_t = sm_f + kMaxGroup * kWarps;                          // [8] 1 / sum, [8] lse
+    if (threadIdx.x < g) {
+        const int h = threadIdx.x;
         float mmax = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
             mmax = fmaxf(mmax, sm_m[w * kMaxGroup + h]);
-        float lsum = 0.f, acc = 0.f;
+        float lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float mw = sm_m[w * kMaxGroup + h];
             const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - mmax);
+            sm_f[h * kWarps + w] = f;
             lsum += sm_l[w * kMaxGroup + h] * f;
-            acc += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * f;
         }
-        const float val = acc / lsum * vscale;
+        sm_t[h] = vscale / lsum;
+        sm_t[kMaxGroup + h] = mmax + __log2f(lsum);
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < kHeadDim; d += kThreads)
+    for (int h = 0; h < g; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            acc += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * sm_f[h * kWarps + w];
+        const float val = acc * sm_t[h];
         const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + hq0 + h;
         if (nsplit == 1) {
             store_out(a.out, bh * kHeadDim + d, val, a.out_fp32);
         } else {
             a.ws_o[(bh * a.max_splits + split) * kHeadDim + d] = val;
             if (d == 0)
-                a.ws_lse[bh * a.max_splits + split] = mmax + __log2f(lsum);
+                a.ws_lse[bh * a.max_splits + split] = sm_t[kMaxGroup + h];
         }
     }
     if (nsplit > 1)

@@ -35,6 +35,10 @@ struct TagCheckArgs {
 };
 cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream);
 
+// Tag check of every request, then the append of token r for request r
+// unless it was aborted (decode step: one new token per request).
+cudaError_t launch_tag_check_append(const TagCheckArgs &t, const AppendArgs &a, cudaStream_t stream);
+
 // Workspace layout (bytes from the workspace base):
 //   [0, counter_bytes)       uint32 arrivals[B][Hkv]: splits of each (request, KV
 //                            head) that have published; zero before the first

@@ -1,0 +1,84 @@
+// kvq_rowops.cuh -- the per-request tag check and the per-row quantise-store
+// shared by the tag-check, append and fused step-prologue kernels.
+#pragma once
+
+#include "kvq_internal.h"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+
+constexpr int kThreadsPerRow = kHeadDim / 8;   // 16 threads x 8 elements per 128-element row
+
+// Tag check of request r by the whole block (blockDim.x threads, kUnroll
+// entries per thread per pass, every block-table and expected-tag load of a
+// pass issued before the live-tag gathers).  Returns the block-wide verdict:
+// true if any used entry names a page outside [0, num_pages) or a page whose
+// live tag differs from the expected one, or if the request needs more
+// entries than its row holds.  Every thread of the block must call it.
+template <int kUnroll>
+__device__ __forceinline__ bool tag_check_request(const int32_t *block_table,
+                                                  const uint32_t *expected_tags,
+                                                  const int32_t *seq_lens, const uint32_t *page_tags,
+                                                  int32_t max_pages_per_seq, int32_t page_size,
+                                                  int32_t num_pages, int64_t r)
+{
+    const int64_t len = seq_lens[r] > 0 ? seq_lens[r] : 0;
+    int64_t used = (len + page_size - 1) / page_size;
+    bool bad = false;
+    if (used > max_pages_per_seq) {
+        bad = true;
+        used = max_pages_per_seq;
+    }
+    const int32_t *bt = block_table + r * max_pages_per_seq;
+    const uint32_t *exp = expected_tags + r * max_pages_per_seq;
+    const int nt = blockDim.x;
+    for (int64_t base = 0; base < used; base += static_cast<int64_t>(nt) * kUnroll) {
+        int32_t p[kUnroll];
+        uint32_t want[kUnroll], live[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int64_t i = base + k * nt + threadIdx.x;
+            p[k] = i < used ? __ldg(bt + i) : 0;
+            want[k] = i < used ? __ldg(exp + i) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const bool in_range = p[k] >= 0 && p[k] < num_pages;
+            live[k] = in_range ? __ldg(page_tags + p[k]) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int64_t i = base + k * nt + threadIdx.x;
+            if (i < used && (p[k] < 0 || p[k] >= num_pages || live[k] != want[k]))
+                bad = true;
+        }
+    }
+    return __syncthreads_or(bad) != 0;
+}
+
+// Eight consecutive elements of one K or V row: bf16 x (16 bytes) becomes
+// eight e4m3 codes e4m3(x / scale) -- one IEEE fp32 division each, rounding
+// to nearest even, saturating at +-448 -- stored as 8 bytes at dst; or, for
+// the bf16 cache, the 16 bytes unchanged.
+template <bool kBf16Cache>
+__device__ __forceinline__ void store_row_part(void *dst_row, int part, uint4 x, float scale)
+{
+    if constexpr (kBf16Cache) {
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst_row) + part * 8) = x;
+    } else {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t packed[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float2 p0 = bf16x2_to_f32x2(w[2 * i]);
+            const float2 p1 = bf16x2_to_f32x2(w[2 * i + 1]);
+            const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(p0.x, scale), __fdiv_rn(p0.y, scale));
+            const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(p1.x, scale), __fdiv_rn(p1.y, scale));
+            packed[i] = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+        }
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(dst_row) + part * 8) =
+            make_uint2(packed[0], packed[1]);
+    }
+}
+
+} // namespace kvq

@@ -13,48 +13,18 @@
 // expected-tag load of the pass before the live-tag gathers, so a pass costs
 // two rounds of dependent loads; OR-reduce with __syncthreads_or; thread 0
 // writes the flag (0 or 1).
-#include "kvq_internal.h"
+#include "kvq_rowops.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kTagThreads = 256;
-constexpr int kTagUnroll = 4;          // entries per thread per pass: all loads issued before any use
 
 __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
 {
     const int64_t r = blockIdx.x;
-    const int64_t len = a.seq_lens[r] > 0 ? a.seq_lens[r] : 0;
-    int64_t used = (len + a.page_size - 1) / a.page_size;
-    bool bad = false;
-    if (used > a.max_pages_per_seq) {
-        bad = true;
-        used = a.max_pages_per_seq;
-    }
-    const int32_t *bt = a.block_table + r * a.max_pages_per_seq;
-    const uint32_t *exp = a.expected_tags + r * a.max_pages_per_seq;
-    for (int64_t base = 0; base < used; base += kTagThreads * kTagUnroll) {
-        int32_t p[kTagUnroll];
-        uint32_t want[kTagUnroll], live[kTagUnroll];
-#pragma unroll
-        for (int k = 0; k < kTagUnroll; ++k) {
-            const int64_t i = base + k * kTagThreads + threadIdx.x;
-            p[k] = i < used ? __ldg(bt + i) : 0;
-            want[k] = i < used ? __ldg(exp + i) : 0u;
-        }
-#pragma unroll
-        for (int k = 0; k < kTagUnroll; ++k) {
-            const bool in_range = p[k] >= 0 && p[k] < a.num_pages;
-            live[k] = in_range ? __ldg(a.page_tags + p[k]) : 0u;
-        }
-#pragma unroll
-        for (int k = 0; k < kTagUnroll; ++k) {
-            const int64_t i = base + k * kTagThreads + threadIdx.x;
-            if (i < used && (p[k] < 0 || p[k] >= a.num_pages || live[k] != want[k]))
-                bad = true;
-        }
-    }
-    bad = __syncthreads_or(bad);
+    const bool bad = tag_check_request<4>(a.block_table, a.expected_tags, a.seq_lens, a.page_tags,
+                                          a.max_pages_per_seq, a.page_size, a.num_pages, r);
     if (threadIdx.x == 0)
         a.abort_flags[r] = bad ? 1 : 0;
 }

@@ -138,6 +138,30 @@ KVQ_API kvq_status kvq_tag_check(const int32_t *block_table, const uint32_t *exp
                          uint8_t *abort_flags, kvq_stream_t stream);
 
 /*
+ * kvq_tag_check_append -- kvq_tag_check followed by kvq_append, fused into
+ * one launch for a decode step in which request r appends exactly one new
+ * token, token r (the page-3 article's check-before-read, then the page-1
+ * article's quantise-on-append).  For every request: the tag check of
+ * kvq_tag_check writes abort_flags[r]; then, only if the request passed,
+ * token r is written as kvq_append would write it.
+ *
+ *   desc, k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache
+ *                  as in kvq_append with num_tokens = batch;
+ *   block_table, expected_tags, seq_lens, batch, max_pages_per_seq,
+ *   page_tags, abort_flags   as in kvq_tag_check (page_size and num_pages
+ *                  come from desc).
+ * Same results as the two calls in sequence.  Supports up to 64 KV heads.
+ */
+KVQ_API kvq_status kvq_tag_check_append(const kvq_cache_desc *desc, const int32_t *block_table,
+                                        const uint32_t *expected_tags, const int32_t *seq_lens,
+                                        int32_t batch, int32_t max_pages_per_seq,
+                                        const uint32_t *page_tags, const void *k_new,
+                                        const void *v_new, const int64_t *slot_mapping,
+                                        const float *k_scale, const float *v_scale,
+                                        void *k_cache, void *v_cache, uint8_t *abort_flags,
+                                        kvq_stream_t stream);
+
+/*
  * kvq_decode_plan -- HOST-only query: how kvq_decode_attn will split the
  * context and how many workspace bytes it needs.
  *

@@ -120,10 +120,20 @@ class DeviceWorkload:
                                    self.v_scale, self.block_table, self.seq_lens,
                                    self.w.softmax_scale, abort, out, workspace, num_splits, stream)
 
-    def step(self, out, workspace, num_splits=0, stream=None):
-        """tag check -> append (skips aborted) -> attention (zeros for aborted)."""
-        self.tag_check(stream)
-        self.append(self.abort, stream)
+    def tag_check_append(self, stream=None):
+        kvq.kvq_tag_check_append(self.desc, self.block_table, self.expected_tags, self.seq_lens,
+                                 self.page_tags, self.k_new, self.v_new, self.append_slots,
+                                 self.k_scale, self.v_scale, self.k_cache, self.v_cache,
+                                 self.abort, stream)
+
+    def step(self, out, workspace, num_splits=0, stream=None, fused=True):
+        """tag check -> append (skips aborted) -> attention (zeros for aborted).
+        fused: the first two as one launch (kvq_tag_check_append)."""
+        if fused:
+            self.tag_check_append(stream)
+        else:
+            self.tag_check(stream)
+            self.append(self.abort, stream)
         return self.attend(out, workspace, self.abort, num_splits, stream)
 
     # ---------------------------------------------------------- oracle feed

@@ -267,3 +267,31 @@ def test_decode_every_e4m3_code_decodes_exactly():
     got = out_to_np(out)
     assert np.array_equal(got[0, 0], dec[:128])
     assert np.array_equal(got[1, 0], dec[126:])
+
+
+# ------------------------------------------------- fused tag check + append
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_tag_check_append_matches_the_two_oracle_passes(bf16):
+    rng = np.random.default_rng(8)
+    w = W.make_custom(rng.integers(1, 900, size=37), group=4, page_size=16, num_kv_heads=8, seed=8)
+    cd = kvq.KVQ_CACHE_BF16 if bf16 else kvq.KVQ_CACHE_FP8_E4M3
+    dw = DeviceWorkload(w, cd)
+    exp = w.expected_tags.copy()
+    exp[3, 0] ^= np.uint32(5)                       # stale: request 3 must be flagged and not written
+    exp[11, -1 + (-(-int(w.seq_lens[11]) // 16))] ^= np.uint32(1)
+    dw.expected_tags.copy_(torch.from_numpy(exp.view(np.int32)))
+    slots = w.append_slot_mapping().copy()
+    slots[5] = -1                                  # skipped token
+    dw.append_slots.copy_(torch.from_numpy(slots))
+    kc_ref, vc_ref = to_np_bits(dw.k_cache), to_np_bits(dw.v_cache)
+    dw.abort.fill_(9)
+    dw.tag_check_append()
+    torch.cuda.synchronize()
+    flags = oracle.tag_check(w.block_table, exp, w.seq_lens, w.page_tags, page_size=16)
+    assert np.array_equal(dw.abort.cpu().numpy(), flags)
+    assert flags[3] == 1 and flags[11] == 1 and flags.sum() == 2
+    oracle.append(kc_ref, vc_ref, to_np_bits(dw.k_new), to_np_bits(dw.v_new), slots,
+                  dw.k_scale_host, dw.v_scale_host, flags, page_size=16)
+    assert np.array_equal(to_np_bits(dw.k_cache), kc_ref)
+    assert np.array_equal(to_np_bits(dw.v_cache), vc_ref)
