@@ -19,6 +19,7 @@ constexpr int kAppendThreads = 256;
 template <bool kBf16Cache>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a)
 {
+    grid_launch_dependents();              // a dependent decode launch may begin now
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (kAppendThreads / kThreadsPerRow) +
                         threadIdx.x / kThreadsPerRow;
     const int part = threadIdx.x % kThreadsPerRow;

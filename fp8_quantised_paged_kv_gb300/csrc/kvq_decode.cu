@@ -218,6 +218,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int g = a.group, ps = a.page_size;
     const int hq0 = kvh * g;                               // first query head of the group
 
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: everything up to here overlaps that kernel; no global memory is
+    // read before the wait.
+    if (threadIdx.x == 0) {
+        prefetch_tensor_map(&k_map);
+        prefetch_tensor_map(&v_map);
+    }
+    grid_dependency_wait();
+
     // The block-table entries this split can use depend only on the split
     // index, so they are loaded together with the request's length.
     const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
@@ -282,10 +291,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const uint32_t part_bytes = static_cast<uint32_t>(box_tok * T::kRowBytes);
     const uint64_t policy = l2_policy_evict_first();
 
-    if (lane == 0) {
-        prefetch_tensor_map(&k_map);
-        prefetch_tensor_map(&v_map);
-    }
 
     // Issue the copies of this warp's local chunk `it` (lane 0 only).
     auto issue = [&](int it) {
@@ -633,7 +638,21 @@ cudaError_t launch_split(const DecodeArgs &a, const CUtensorMap &k_map, const CU
     }
     const dim3 grid(static_cast<unsigned>(a.max_splits), static_cast<unsigned>(a.num_kv_heads),
                     static_cast<unsigned>(a.batch));
-    decode_split_kernel<kBf16, kPrecise><<<grid, kThreads, T::kSmemBytes, stream>>>(k_map, v_map, a);
+    // programmatic dependent launch: the grid may start while the previous
+    // kernel on the stream finishes; the kernel waits before its first read
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_split_kernel<kBf16, kPrecise>, k_map, v_map, a);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

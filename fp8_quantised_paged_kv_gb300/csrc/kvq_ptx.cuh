@@ -209,4 +209,18 @@ __device__ __forceinline__ void prefetch_tensor_map(const void *tensor_map)
                  : "memory");
 }
 
+// Programmatic dependent launch.  wait: block until the grids this grid
+// depends on have completed and their writes are visible (a no-op when the
+// grid was not launched as a dependent).  launch_dependents: let the next
+// grid on the stream start launching now.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 } // namespace kvq

@@ -21,6 +21,7 @@ constexpr int kMaxRowsPerPass = kStepThreads / kThreadsPerRow;   // 16 rows (K a
 template <bool kBf16Cache>
 __global__ void __launch_bounds__(kStepThreads) tag_check_append_kernel(TagCheckArgs t, AppendArgs a)
 {
+    grid_launch_dependents();              // a dependent decode launch may begin now
     const int64_t r = blockIdx.x;
     const int rows = 2 * a.num_kv_heads;
     const int part = threadIdx.x % kThreadsPerRow;

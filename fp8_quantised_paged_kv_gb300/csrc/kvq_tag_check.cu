@@ -22,6 +22,7 @@ constexpr int kTagThreads = 256;
 
 __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
 {
+    grid_launch_dependents();              // a dependent decode launch may begin now
     const int64_t r = blockIdx.x;
     const bool bad = tag_check_request<4>(a.block_table, a.expected_tags, a.seq_lens, a.page_tags,
                                           a.max_pages_per_seq, a.page_size, a.num_pages, r);
