@@ -36,9 +36,10 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_uniform8.json")
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources of the decode kernel (the one the roofline reports)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quantised_paged_kv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("kvq_decode.cu", "kvq_ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

@@ -62,6 +62,8 @@ _SIGS = {
     "kvq_decode_attn": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
                         "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
+    "kvq_amax_scales": ["desc", "p", "p", "p", "i32", "p", "p", "p"],
+    "kvq_quantize_pages": ["desc", "p", "p", "p", "desc", "p", "p", "p", "i32", "p", "p", "p"],
     "kvq_tag_check_append": ["desc", "p", "p", "p", "i32", "i32", "p", "p", "p", "p", "p", "p",
                              "p", "p", "p", "p"],
     "kvq_decode_attn_static_ws": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p",
@@ -177,6 +179,30 @@ def kvq_tag_check_append(desc: CacheDesc, block_table, expected_tags, seq_lens, 
         _ptr(page_tags), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_scale),
         _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), _ptr(abort_flags), _stream(stream))
     _check("kvq_tag_check_append", st)
+
+
+def kvq_amax_scales(desc: CacheDesc, k_cache, v_cache, pages, k_scale, v_scale, stream=None):
+    """Per-KV-head scales amax / 448 of the listed pages of bf16 caches (written into k_scale, v_scale)."""
+    import torch
+    _expect(pages, torch.int32, None, "pages")
+    _expect(k_scale, torch.float32, (desc.num_kv_heads,), "k_scale")
+    _expect(v_scale, torch.float32, (desc.num_kv_heads,), "v_scale")
+    st = load().kvq_amax_scales(ctypes.byref(desc.c()), _ptr(k_cache), _ptr(v_cache), _ptr(pages),
+                                pages.numel(), _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    _check("kvq_amax_scales", st)
+
+
+def kvq_quantize_pages(src_desc: CacheDesc, k_src, v_src, src_pages, dst_desc: CacheDesc, k_dst,
+                       v_dst, dst_pages, k_scale, v_scale, stream=None):
+    """bf16 pages src_pages[i] -> e4m3 pages dst_pages[i], per-KV-head scales."""
+    import torch
+    _expect(src_pages, torch.int32, None, "src_pages")
+    _expect(dst_pages, torch.int32, (src_pages.numel(),), "dst_pages")
+    st = load().kvq_quantize_pages(ctypes.byref(src_desc.c()), _ptr(k_src), _ptr(v_src),
+                                   _ptr(src_pages), ctypes.byref(dst_desc.c()), _ptr(k_dst),
+                                   _ptr(v_dst), _ptr(dst_pages), src_pages.numel(), _ptr(k_scale),
+                                   _ptr(v_scale), _stream(stream))
+    _check("kvq_quantize_pages", st)
 
 
 def kvq_decode_plan(desc: CacheDesc, batch: int, num_q_heads: int, max_pages_per_seq: int,

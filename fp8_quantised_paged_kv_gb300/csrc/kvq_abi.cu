@@ -376,6 +376,70 @@ kvq_status kvq_tag_check_append(const kvq_cache_desc *desc, const int32_t *block
     return to_status(kvq::launch_tag_check_append(t, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_amax_scales(const kvq_cache_desc *desc, const void *k_cache, const void *v_cache,
+                           const int32_t *pages, int32_t num_listed, float *k_scale,
+                           float *v_scale, kvq_stream_t stream)
+{
+    kvq_status st = check_desc(desc);
+    if (st != KVQ_OK)
+        return st;
+    if (desc->cache_dtype != KVQ_CACHE_BF16)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_listed < 0 || !k_scale || !v_scale || (num_listed > 0 && (!k_cache || !v_cache || !pages)))
+        return KVQ_ERR_INVALID_ARG;
+    if (num_listed > 0 && (!aligned16(k_cache) || !aligned16(v_cache)))
+        return KVQ_ERR_INVALID_ARG;
+    kvq::HandoffArgs a = {};
+    a.k_src = k_cache;
+    a.v_src = v_cache;
+    a.src_pages = pages;
+    a.k_scale_out = k_scale;
+    a.v_scale_out = v_scale;
+    a.num_listed = num_listed;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.page_size = desc->page_size;
+    a.src_num_pages = desc->num_pages;
+    return to_status(kvq::launch_amax_scales(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_quantize_pages(const kvq_cache_desc *src_desc, const void *k_src, const void *v_src,
+                              const int32_t *src_pages, const kvq_cache_desc *dst_desc, void *k_dst,
+                              void *v_dst, const int32_t *dst_pages, int32_t num_listed,
+                              const float *k_scale, const float *v_scale, kvq_stream_t stream)
+{
+    kvq_status st = check_desc(src_desc);
+    if (st == KVQ_OK)
+        st = check_desc(dst_desc);
+    if (st != KVQ_OK)
+        return st;
+    if (src_desc->cache_dtype != KVQ_CACHE_BF16 || dst_desc->cache_dtype != KVQ_CACHE_FP8_E4M3 ||
+        src_desc->page_size != dst_desc->page_size || src_desc->num_kv_heads != dst_desc->num_kv_heads)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_listed < 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_listed == 0)
+        return KVQ_OK;
+    if (!k_src || !v_src || !src_pages || !k_dst || !v_dst || !dst_pages || !k_scale || !v_scale)
+        return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_dst) || !aligned16(v_dst))
+        return KVQ_ERR_INVALID_ARG;
+    kvq::HandoffArgs a = {};
+    a.k_src = k_src;
+    a.v_src = v_src;
+    a.src_pages = src_pages;
+    a.k_dst = k_dst;
+    a.v_dst = v_dst;
+    a.dst_pages = dst_pages;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.num_listed = num_listed;
+    a.num_kv_heads = src_desc->num_kv_heads;
+    a.page_size = src_desc->page_size;
+    a.src_num_pages = src_desc->num_pages;
+    a.dst_num_pages = dst_desc->num_pages;
+    return to_status(kvq::launch_quantize_pages(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
                            int32_t max_pages_per_seq, int32_t num_splits, int32_t *split_tokens,
                            int32_t *max_splits, size_t *workspace_bytes)

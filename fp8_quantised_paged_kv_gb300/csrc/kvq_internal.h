@@ -35,6 +35,19 @@ struct TagCheckArgs {
 };
 cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream);
 
+// Prefill -> decode handoff of whole pages (bf16 source, e4m3 destination).
+struct HandoffArgs {
+    const void *k_src, *v_src;              // bf16 caches [src_num_pages][Hkv][ps][D]
+    const int32_t *src_pages;               // [num_listed]
+    void *k_dst, *v_dst;                    // e4m3 caches [dst_num_pages][Hkv][ps][D]
+    const int32_t *dst_pages;               // [num_listed]
+    const float *k_scale, *v_scale;         // [Hkv] (quantise)
+    float *k_scale_out, *v_scale_out;       // [Hkv] (amax -> scale)
+    int32_t num_listed, num_kv_heads, page_size, src_num_pages, dst_num_pages;
+};
+cudaError_t launch_amax_scales(const HandoffArgs &a, cudaStream_t stream);
+cudaError_t launch_quantize_pages(const HandoffArgs &a, cudaStream_t stream);
+
 // Tag check of every request, then the append of token r for request r
 // unless it was aborted (decode step: one new token per request).
 cudaError_t launch_tag_check_append(const TagCheckArgs &t, const AppendArgs &a, cudaStream_t stream);

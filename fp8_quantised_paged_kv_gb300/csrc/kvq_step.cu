@@ -15,8 +15,8 @@
 namespace kvq {
 namespace {
 
-constexpr int kStepThreads = 256;
-constexpr int kMaxRowsPerPass = kStepThreads / kThreadsPerRow;   // 16 rows (K and V of 8 heads)
+constexpr int kStepThreads = 512;
+constexpr int kMaxRowsPerPass = kStepThreads / kThreadsPerRow;   // 32 rows (K and V of 16 heads)
 
 template <bool kBf16Cache>
 __global__ void __launch_bounds__(kStepThreads) tag_check_append_kernel(TagCheckArgs t, AppendArgs a)
@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kStepThreads) tag_check_append_kernel(TagCheck
     }
     const int64_t slot = __ldg(a.slot_mapping + r);
 
-    const bool bad = tag_check_request<4>(t.block_table, t.expected_tags, t.seq_lens, t.page_tags,
+    const bool bad = tag_check_request<8>(t.block_table, t.expected_tags, t.seq_lens, t.page_tags,
                                           t.max_pages_per_seq, t.page_size, t.num_pages, r);
     if (threadIdx.x == 0)
         t.abort_flags[r] = bad ? 1 : 0;

@@ -8,8 +8,8 @@
 // (blog post "Smaller, faster, safer", page-2 mirror section "KV Cache
 // 完整性检查"; page-3 mirror section "一个不能出错的共享缓存").
 //
-// One CTA per request: its 256 threads take the ceil(L / page_size) entries
-// the request uses, 1,024 per pass, issuing every block-table and
+// One CTA per request: its 512 threads take the ceil(L / page_size) entries
+// the request uses, 4,096 per pass, issuing every block-table and
 // expected-tag load of the pass before the live-tag gathers, so a pass costs
 // two rounds of dependent loads; OR-reduce with __syncthreads_or; thread 0
 // writes the flag (0 or 1).
@@ -18,13 +18,13 @@
 namespace kvq {
 namespace {
 
-constexpr int kTagThreads = 256;
+constexpr int kTagThreads = 512;
 
 __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
 {
     grid_launch_dependents();              // a dependent decode launch may begin now
     const int64_t r = blockIdx.x;
-    const bool bad = tag_check_request<4>(a.block_table, a.expected_tags, a.seq_lens, a.page_tags,
+    const bool bad = tag_check_request<8>(a.block_table, a.expected_tags, a.seq_lens, a.page_tags,
                                           a.max_pages_per_seq, a.page_size, a.num_pages, r);
     if (threadIdx.x == 0)
         a.abort_flags[r] = bad ? 1 : 0;

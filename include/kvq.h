@@ -162,6 +162,38 @@ KVQ_API kvq_status kvq_tag_check_append(const kvq_cache_desc *desc, const int32_
                                         kvq_stream_t stream);
 
 /*
+ * Prefill -> decode handoff.  Prefill is compute-bound and keeps its cache in
+ * BF16; the decode pool stores FP8 (page-1 article, section "量化KV缓存";
+ * page-2 summary, section "KV Cache 量化以提高并发量").  Pages that move
+ * from a prefill (bf16) cache to a decode (e4m3) cache are quantised whole.
+ *
+ * kvq_amax_scales -- per-KV-head scales of a set of bf16 pages:
+ *   k_scale[h] = amax_h / 448 (one IEEE fp32 division), amax_h = max |x|
+ *   over head h of every listed page of k_cache (1 when amax_h is 0); same
+ *   for V.  desc describes the bf16 caches; pages int32 [num_listed];
+ *   k_scale, v_scale fp32 [Hkv] OUTPUT (device).  Listed ids outside
+ *   [0, num_pages) are ignored.
+ */
+KVQ_API kvq_status kvq_amax_scales(const kvq_cache_desc *desc, const void *k_cache,
+                                   const void *v_cache, const int32_t *pages, int32_t num_listed,
+                                   float *k_scale, float *v_scale, kvq_stream_t stream);
+
+/*
+ * kvq_quantize_pages -- bf16 page src_pages[i] of (k_src, v_src) becomes
+ * e4m3 page dst_pages[i] of (k_dst, v_dst): every element e4m3(x / scale[h])
+ * by the kvq_append rule (fp32 division, round to nearest even, saturate at
+ * +-448).  src_desc must be a bf16 cache and dst_desc an e4m3 cache with the
+ * same page size and KV-head count.  A pair with an out-of-range source or
+ * destination id is skipped; destination pages listed twice race.
+ */
+KVQ_API kvq_status kvq_quantize_pages(const kvq_cache_desc *src_desc, const void *k_src,
+                                      const void *v_src, const int32_t *src_pages,
+                                      const kvq_cache_desc *dst_desc, void *k_dst, void *v_dst,
+                                      const int32_t *dst_pages, int32_t num_listed,
+                                      const float *k_scale, const float *v_scale,
+                                      kvq_stream_t stream);
+
+/*
  * kvq_decode_plan -- HOST-only query: how kvq_decode_attn will split the
  * context and how many workspace bytes it needs.
  *

@@ -74,6 +74,10 @@ def _load():
     lib.oracle_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P,
                                        P, i32, P, ctypes.c_float, P, P]
     lib.oracle_decode_attn.restype = None
+    lib.oracle_amax_scales.argtypes = [i32, i32, i32, P, P, P, i32, P, P]
+    lib.oracle_amax_scales.restype = None
+    lib.oracle_quantize_pages.argtypes = [i32, i32, i32, P, P, P, P, P, P, i32, P, P]
+    lib.oracle_quantize_pages.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     _lib = lib
@@ -178,3 +182,32 @@ def decode_attn(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                            _ptr(v_cache), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
                            _ptr(sl), ctypes.c_float(softmax_scale), _ptr(ab), _ptr(out))
     return out
+
+
+def amax_scales(k_cache, v_cache, pages):
+    """Per-KV-head (k_scale, v_scale): amax / 448 over the listed bf16 pages (1 if amax is 0)."""
+    lib = _load()
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    assert kc.dtype == np.uint16 and vc.dtype == np.uint16
+    N, Hkv, ps, D = kc.shape
+    pg = _c(pages, np.int32)
+    ks = np.empty(Hkv, np.float32)
+    vs = np.empty(Hkv, np.float32)
+    lib.oracle_amax_scales(Hkv, D, ps, _ptr(kc), _ptr(vc), _ptr(pg), pg.size, _ptr(ks), _ptr(vs))
+    return ks, vs
+
+
+def quantize_pages(k_src, v_src, src_pages, k_dst, v_dst, dst_pages, k_scale, v_scale):
+    """In-place: bf16 pages src_pages[i] -> e4m3 pages dst_pages[i] of k_dst/v_dst."""
+    lib = _load()
+    ks_ = np.ascontiguousarray(k_src)
+    vs_ = np.ascontiguousarray(v_src)
+    N, Hkv, ps, D = ks_.shape
+    assert k_dst.dtype == np.uint8 and k_dst.flags.c_contiguous and v_dst.flags.c_contiguous
+    sp = _c(src_pages, np.int32)
+    dp = _c(dst_pages, np.int32)
+    assert sp.size == dp.size
+    lib.oracle_quantize_pages(Hkv, D, ps, _ptr(ks_), _ptr(vs_), _ptr(sp), _ptr(k_dst), _ptr(v_dst),
+                              _ptr(dp), sp.size, _ptr(_c(k_scale, np.float32)),
+                              _ptr(_c(v_scale, np.float32)))

@@ -314,3 +314,58 @@ int32_t oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------ prefill -> decode */
+
+/*
+ * Per-KV-head scales of a set of bf16 pages: scale[h] = amax / 448 over
+ * every element of head h in the listed pages (one fp32 division), 1 when
+ * amax is 0.  K and V separately.  (Prefill keeps a BF16 cache and decode an
+ * FP8 one: page 1 "量化KV缓存"; these scales are what the decode pool
+ * quantises the handed-over pages with.)
+ */
+void oracle_amax_scales(int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                        const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *pages, int32_t n_pages,
+                        float *k_scale, float *v_scale)
+{
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+        float ka = 0.0f, va = 0.0f;
+        for (int32_t i = 0; i < n_pages; ++i) {
+            int64_t base = ((int64_t)pages[i] * num_kv_heads + h) * page_size * head_dim;
+            for (int64_t e = 0; e < (int64_t)page_size * head_dim; ++e) {
+                float kx = fabsf(bf16_bits_to_float(k_cache[base + e]));
+                float vx = fabsf(bf16_bits_to_float(v_cache[base + e]));
+                if (kx > ka)
+                    ka = kx;
+                if (vx > va)
+                    va = vx;
+            }
+        }
+        k_scale[h] = ka > 0.0f ? ka / 448.0f : 1.0f;
+        v_scale[h] = va > 0.0f ? va / 448.0f : 1.0f;
+    }
+}
+
+/*
+ * Quantise whole bf16 pages into e4m3 pages: element (h, slot, d) of page
+ * src_pages[i] becomes encode((float)x / scale[h]) at the same position of
+ * page dst_pages[i] -- the append rule applied to every slot of the page.
+ */
+void oracle_quantize_pages(int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                           const uint16_t *k_src, const uint16_t *v_src, const int32_t *src_pages,
+                           uint8_t *k_dst, uint8_t *v_dst, const int32_t *dst_pages, int32_t n,
+                           const float *k_scale, const float *v_scale)
+{
+    const int64_t per_head = (int64_t)page_size * head_dim;
+    for (int32_t i = 0; i < n; ++i) {
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            int64_t s = ((int64_t)src_pages[i] * num_kv_heads + h) * per_head;
+            int64_t d = ((int64_t)dst_pages[i] * num_kv_heads + h) * per_head;
+            for (int64_t e = 0; e < per_head; ++e) {
+                k_dst[d + e] = oracle_e4m3_encode(bf16_bits_to_float(k_src[s + e]) / k_scale[h]);
+                v_dst[d + e] = oracle_e4m3_encode(bf16_bits_to_float(v_src[s + e]) / v_scale[h]);
+            }
+        }
+    }
+}
