@@ -404,6 +404,72 @@ def run_ours(args):
     return 0
 
 
+def run_churn(args):
+    """32-layer churn workload: per step one tag check, then for every layer
+    the append of each request's new token and the decode attention.  Reports
+    the KV bytes the step reads per second and the tag check's share of the
+    step time (the pages' integrity-check overhead figure)."""
+    import torch
+    import fp8_quantised_paged_kv_gb300 as kvq
+    from kvq_churn import ChurnDevice, ChurnState
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    kvq.load()
+    kvq.kvq_device_error(clear=True)
+    st = ChurnState(seed=rank)
+    dev = ChurnDevice(st, layers=32, device=f"cuda:{local}", log_layers=())
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
+    rows = []
+    for i in range(args.warmup + args.steps):
+        bt, exp, seq, stale = st.tables()
+        bt_d, exp_d, seq_d, tags_d, slots, slots_d = dev.upload(bt, exp, seq)
+        vals = [dev.step_values(l, st.step_index) for l in range(dev.layers)]
+        outs = [torch.empty((st.batch, dev.hq, dev.D), dtype=torch.bfloat16, device=dev.device)
+                for _ in range(dev.layers)]
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        kvq.kvq_tag_check(bt_d, exp_d, seq_d, st.ps, tags_d, dev.abort)
+        e[1].record(stream)
+        for l in range(dev.layers):
+            q, kn, vn = vals[l]
+            kvq.kvq_append(dev.desc, kn, vn, slots_d, dev.k_scale[l], dev.v_scale[l], dev.abort,
+                           dev.k[l], dev.v[l])
+            kvq.kvq_decode_attn(dev.desc, q, dev.k[l], dev.v[l], dev.k_scale[l], dev.v_scale[l],
+                                bt_d, seq_d, dev.sigma, dev.abort, outs[l], dev.ws)
+        e[2].record(stream)
+        abort = dev.abort.cpu().numpy()
+        live = (seq > 0) & (abort == 0)
+        kv_bytes = int(seq[live].astype(np.int64).sum()) * dev.hkv * 256 * dev.layers
+        if i >= args.warmup:
+            rows.append((e[0], e[1], e[2], kv_bytes, int(live.sum())))
+        st.advance(set(np.nonzero(abort)[0].tolist()))
+    torch.cuda.synchronize()
+    tag = np.array([a.elapsed_time(b) for a, b, _, _, _ in rows])
+    step = np.array([a.elapsed_time(c) for a, _, c, _, _ in rows])
+    kvb = np.array([r[3] for r in rows], np.float64)
+    reqs = np.array([r[4] for r in rows], np.float64)
+    value = float(kvb.sum() / (step.sum() / 1e3) / 1e9)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(float(step.mean()), 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+            "data": "synthetic",
+            "config": {"workload": "churn", "layers": 32, "batch": st.batch, "num_q_heads": dev.hq,
+                       "num_kv_heads": dev.hkv, "page_size": st.ps,
+                       "l2": "flushed before every timed step (512 MiB write)",
+                       "step": "tag check once, then 32 x (append + decode attention)"},
+            "tokens_per_s": round(float(reqs.sum() / (step.sum() / 1e3)), 1),
+            "tag_check_us": round(float(tag.mean() * 1e3), 2),
+            "tag_check_share_of_step": round(float(tag.sum() / step.sum()), 6),
+            "device_error_bits": kvq.kvq_device_error(),
+        }))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,6 +486,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "churn":
+        return run_churn(args)
     return run_ours(args)
 
 
