@@ -255,8 +255,12 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     kv_bytes = w.kv_bytes(1)
-    split_tokens, max_splits, _ = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads,
-                                                      w.max_pages_per_seq, args.num_splits)
+    split_tokens, max_splits, ws_bytes = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads,
+                                                             w.max_pages_per_seq, args.num_splits)
+    counter_bytes = (w.batch * w.num_kv_heads * 4 + 255) // 256 * 256
+    combine = ("none" if max_splits == 1 else
+               "cluster (distributed shared memory)" if ws_bytes == counter_bytes else
+               "workspace (last-arriving split)")
 
     def step(ev=None):
         if ev is not None:
@@ -276,7 +280,10 @@ def run_ours(args):
             step()
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Timed steps: events only at the step boundaries.  An event recorded
+    # between the two launches would stop the decode kernel from starting
+    # as a programmatic dependent of the step prologue.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -285,17 +292,30 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.zero_()                 # L2 flushed before every timed step
-            step(evs[i])
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     t_wall = t_wall1 - t_wall0
     sampler.stop()
     if world > 1:
         dist.barrier()
-    parts = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(2)]
-                      for i in range(args.steps)])          # ms
-    agg = aggregate_ranks(float(parts.sum(axis=1).mean()), kv_bytes, w.batch, device=dev)
+    step_times = np.array([e[0].elapsed_time(e[1]) for e in evs])       # ms
+    agg = aggregate_ranks(float(step_times.mean()), kv_bytes, w.batch, device=dev)
     step_ms = agg["ms_per_step"]
+
+    # Per-kernel durations (same flush before every step), events around each
+    # of the two launches; the decode kernel's is the roofline's denominator.
+    k_steps = max(3, min(args.steps, 1000))
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k_steps)]
+    with torch.cuda.stream(stream):
+        for i in range(k_steps):
+            flush.zero_()
+            step(kev[i])
+    torch.cuda.synchronize()
+    parts = np.array([[kev[i][j].elapsed_time(kev[i][j + 1]) for j in range(2)]
+                      for i in range(k_steps)])             # ms
     pre_ms, attn_ms = (float(x) for x in parts.mean(axis=0))
 
     # ---- end to end: host (pinned) inputs -> device -> step -> host result
@@ -377,6 +397,7 @@ def run_ours(args):
                        "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                        "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3",
                        "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
+                       "split_combine": combine,
                        "l2": "flushed before every timed step (512 MiB write)",
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": round(agg["tokens_per_s"], 1),

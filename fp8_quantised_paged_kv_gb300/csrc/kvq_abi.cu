@@ -56,6 +56,7 @@ kvq_status check_desc(const kvq_cache_desc *d)
 
 struct Plan {
     int32_t split_tokens, max_splits;
+    int32_t cluster;              // 0, or the cluster size (= max_splits) of the cluster combine
     size_t counter_bytes, lse_bytes, o_bytes;
 };
 
@@ -116,6 +117,18 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     }
     if (want < 1)
         want = 1;
+    const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
+    const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads;
+    if (num_splits == 0 && want >= 2 && batch > 0) {
+        // A job whose splits could all be resident as clusters merges them
+        // through distributed shared memory, a much shorter tail than the
+        // workspace combine; that is worth giving up up to half the splits.
+        int64_t c = want < kvq::kMaxCluster ? want : kvq::kMaxCluster;
+        while (c >= 2 && pairs > kvq::decode_cluster_capacity(static_cast<int>(c), bf16))
+            --c;
+        if (c >= 2 && 2 * c >= want)
+            want = c;
+    }
     int64_t split = (max_ctx + want - 1) / want;
     split = (split + unit - 1) / unit * unit;
     if (split > kMaxSplitTokens)
@@ -125,10 +138,17 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         return KVQ_ERR_UNSUPPORTED;
     p->split_tokens = static_cast<int32_t>(split);
     p->max_splits = static_cast<int32_t>(splits);
+    // When every (request, KV head) fits in one resident cluster of `splits`
+    // CTAs, the splits merge through distributed shared memory instead of
+    // the workspace.
+    p->cluster = 0;
+    if (splits >= 2 && batch > 0 &&
+        pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16))
+        p->cluster = static_cast<int32_t>(splits);
     p->counter_bytes = (static_cast<size_t>(batch) * d->num_kv_heads * 4 + 255) / 256 * 256;
     if (p->counter_bytes == 0)
         p->counter_bytes = 256;
-    if (splits > 1) {
+    if (splits > 1 && p->cluster == 0) {
         const size_t n = static_cast<size_t>(batch) * num_q_heads * splits;
         p->lse_bytes = (n * sizeof(float) + 255) / 256 * 256;
         p->o_bytes = n * kHeadDim * sizeof(float);
@@ -242,6 +262,7 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     a.max_pages_per_seq = max_pages_per_seq;
     a.split_tokens = call->plan.split_tokens;
     a.max_splits = call->plan.max_splits;
+    a.cluster = call->plan.cluster;
     a.qk_scale_log2 = softmax_scale * 1.4426950408889634f;
     a.out_fp32 = out_dtype == KVQ_OUT_FP32;
     a.bf16_cache = bf16;

@@ -24,6 +24,9 @@
 // the (request, KV head) to finish merges them all (the combine), counted by
 // a per-(request, KV head) arrival counter that it resets to zero.
 #include <cfloat>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include <cuda_bf16.h>
 
@@ -43,6 +46,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // give up on a copy after ~1 s
 constexpr int kMaxSplits = 1024;
+constexpr int kPrefetchTokens = 256;             // per split, requested into L2 before the wait
 
 template <bool kBf16Cache>
 struct Tile {
@@ -97,6 +101,8 @@ __device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool 
 // warps' merge area, inside the ring (idle by then).
 constexpr int kScratchOffset =
     (kWarps * kMaxGroup * kHeadDim + 3 * kWarps * kMaxGroup + 2 * kMaxGroup + 3) / 4 * 4;
+static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kHeadDim) * 4 <= Tile<false>::kRingBytes,
+              "combine scratch and cluster partial fit in the idle ring");
 
 // Count this split's arrival for (request b, KV head kvh).  The last split
 // to arrive merges the partials of all nsplit splits of the group:
@@ -199,7 +205,65 @@ __device__ void drop_split(const DecodeArgs &a, int b, int kvh, int split, int n
     publish_and_combine(a, b, kvh, nsplit, smem + kScratchOffset);
 }
 
-template <bool kBf16Cache, bool kPreciseP>
+// What a split contributes to the cluster form of the combine.
+enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2 };
+
+// Cluster form of the combine, used when the splits of each (request, KV
+// head) are the CTAs of one thread-block cluster (every split resident at
+// once).  Each CTA leaves its partial in its own shared memory at `part`:
+// [kMaxGroup] lse (log2 domain), then [kMaxGroup][128] normalised o; an empty
+// split (no tokens) publishes lse = -inf (weight 0), an invalid one NaN (its
+// heads get zeros).  After a cluster barrier CTA r merges the query heads
+// h = r, r + n, ... of the group from every peer's partial, read through
+// distributed shared memory:
+//   M = max_s lse_s,  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).
+// A second barrier keeps every CTA's shared memory alive until its peers
+// have read it.  Every CTA of the cluster calls this exactly once.
+__device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part)
+{
+    static_assert(kThreads == kHeadDim, "one thread per output dimension");
+    if (status != kPartialOk && threadIdx.x < kMaxGroup)
+        part[threadIdx.x] = status == kPartialEmpty ? -INFINITY : __int_as_float(0x7FC00000);
+    cluster_sync();
+    const int g = a.group, n = a.max_splits;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const uint32_t base = smem_addr(part);
+    const int d = threadIdx.x;
+    for (int h = rank; h < g; h += n) {
+        float lse[kMaxCluster], ov[kMaxCluster];
+#pragma unroll
+        for (int s = 0; s < kMaxCluster; ++s) {
+            lse[s] = -INFINITY;
+            ov[s] = 0.f;
+            if (s < n) {
+                const uint32_t peer = map_shared_rank(base, static_cast<uint32_t>(s));
+                lse[s] = ld_shared_cluster_f32(peer + 4u * h);
+                ov[s] = ld_shared_cluster_f32(peer + 4u * (kMaxGroup + h * kHeadDim + d));
+            }
+        }
+        float m = -INFINITY;
+        bool bad = false;
+#pragma unroll
+        for (int s = 0; s < kMaxCluster; ++s) {
+            bad |= lse[s] != lse[s];
+            m = fmaxf(m, lse[s]);
+        }
+        float sum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMaxCluster; ++s) {
+            if (lse[s] != -INFINITY) {
+                const float w = fast_exp2(lse[s] - m);
+                sum += w;
+                acc += w * ov[s];
+            }
+        }
+        store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * kHeadDim + d,
+                  (bad || !(sum > 0.f)) ? 0.f : acc / sum, a.out_fp32);
+    }
+    cluster_sync();
+}
+
+template <bool kBf16Cache, bool kPreciseP, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a)
@@ -218,21 +282,45 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int g = a.group, ps = a.page_size;
     const int hq0 = kvh * g;                               // first query head of the group
 
+    const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
+    const int span_left = a.max_pages_per_seq - first_page;
+    const int span = a.split_tokens / ps < span_left ? a.split_tokens / ps : span_left;
+    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
+    const int lines_per_tok = kBf16Cache ? 2 : 1;
+
     // Launched as a programmatic dependent of the previous kernel on the
-    // stream: everything up to here overlaps that kernel; no global memory is
-    // read before the wait.
+    // stream: everything up to the wait overlaps that kernel.  Meanwhile the
+    // split's first kPrefetchTokens tokens are requested into L2, so HBM is
+    // busy before the wait returns.  Values read here only steer those L2
+    // prefetches (hints that L2 keeps coherent with every write): a
+    // block-table entry the previous kernel is still writing costs at most a
+    // useless prefetch.  Everything the split computes with is read after
+    // the wait.
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&k_map);
         prefetch_tensor_map(&v_map);
+    }
+    {
+        const int box_tok = ps < kChunkTokens ? ps : kChunkTokens;
+        const int boxes = kPrefetchTokens / box_tok;
+        for (int i = threadIdx.x; i < boxes; i += kThreads) {
+            const int tok = i * box_tok;                   // from the split's start
+            const int pi = tok / ps;
+            if (pi < span) {
+                const int32_t id = __ldcg(bt + pi);       // L2 only: no stale copy in L1
+                if (id >= 0 && id < a.num_pages) {
+                    const int64_t row = (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * ps + tok % ps;
+                    const int32_t y = static_cast<int32_t>(row * lines_per_tok);
+                    tma_prefetch_l2_2d(&k_map, 0, y);
+                    tma_prefetch_l2_2d(&v_map, 0, y);
+                }
+            }
+        }
     }
     grid_dependency_wait();
 
     // The block-table entries this split can use depend only on the split
     // index, so they are loaded together with the request's length.
-    const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
-    const int span_left = a.max_pages_per_seq - first_page;
-    const int span = a.split_tokens / ps < span_left ? a.split_tokens / ps : span_left;
-    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
     constexpr int kIdsPerThread = (kMaxPageList + kThreads - 1) / kThreads;
     int32_t ids[kIdsPerThread];
 #pragma unroll
@@ -245,6 +333,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int64_t cap = static_cast<int64_t>(a.max_pages_per_seq) * ps;
     const bool zero_request = aborted || len <= 0 || len > cap;
     const int nsplit = zero_request ? 1 : static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
+    float *part = reinterpret_cast<float *>(smem) + kScratchOffset;   // cluster partial
+    if constexpr (kCluster) {
+        if (zero_request || split >= nsplit) {             // no tokens: weight 0
+            cluster_finish(a, b, kvh, kPartialEmpty, part);
+            return;
+        }
+    }
     if (split >= nsplit)
         return;
 
@@ -276,7 +371,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     bad = __syncthreads_or(bad);
     if (bad) {
-        drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
+        if constexpr (kCluster)
+            cluster_finish(a, b, kvh, kPartialInvalid, part);
+        else
+            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
         return;
     }
 
@@ -287,7 +385,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     uint64_t *my_full = full + warp * T::kStages;
     const int box_tok = ps < kChunkTokens ? ps : kChunkTokens;
     const int parts = kChunkTokens / box_tok;                       // 1 or 2 copies per tensor
-    const int lines_per_tok = kBf16Cache ? 2 : 1;
     const uint32_t part_bytes = static_cast<uint32_t>(box_tok * T::kRowBytes);
     const uint64_t policy = l2_policy_evict_first();
 
@@ -550,7 +647,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     __syncthreads();
     if (s_failed) {
-        drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
+        if constexpr (kCluster)
+            cluster_finish(a, b, kvh, kPartialInvalid, part);
+        else
+            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
         return;
     }
 
@@ -607,7 +707,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             acc += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * sm_f[h * kWarps + w];
         const float val = acc * sm_t[h];
         const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + hq0 + h;
-        if (nsplit == 1) {
+        if constexpr (kCluster) {
+            part[kMaxGroup + h * kHeadDim + d] = val;
+            if (d == 0)
+                part[h] = sm_t[kMaxGroup + h];
+        } else if (nsplit == 1) {
             store_out(a.out, bh * kHeadDim + d, val, a.out_fp32);
         } else {
             a.ws_o[(bh * a.max_splits + split) * kHeadDim + d] = val;
@@ -615,45 +719,103 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 a.ws_lse[bh * a.max_splits + split] = sm_t[kMaxGroup + h];
         }
     }
-    if (nsplit > 1)
+    if constexpr (kCluster)
+        cluster_finish(a, b, kvh, kPartialOk, part);
+    else if (nsplit > 1)
         publish_and_combine(a, b, kvh, nsplit, reinterpret_cast<float *>(smem) + kScratchOffset);
 }
 
-template <bool kBf16, bool kPrecise>
+template <bool kBf16, bool kPrecise, bool kCluster>
+cudaError_t configure(int dev)
+{
+    static int configured[64] = {0};
+    if (dev >= 0 && dev < 64 && configured[dev])
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kBf16, kPrecise, kCluster>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tile<kBf16>::kSmemBytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        configured[dev] = 1;
+    return e;
+}
+
+template <bool kBf16, bool kPrecise, bool kCluster>
+cudaLaunchConfig_t launch_config(const DecodeArgs &a, dim3 grid, cudaStream_t stream,
+                                 cudaLaunchAttribute (&attr)[2])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Tile<kBf16>::kSmemBytes;
+    cfg.stream = stream;
+    // programmatic dependent launch: the grid may start while the previous
+    // kernel on the stream finishes; the kernel waits before its first read
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (kCluster) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(a.max_splits);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
+    return cfg;
+}
+
+template <bool kBf16, bool kPrecise, bool kCluster>
 cudaError_t launch_split(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                          cudaStream_t stream)
 {
-    using T = Tile<kBf16>;
-    static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<kBf16, kPrecise>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
+    e = configure<kBf16, kPrecise, kCluster>(dev);
+    if (e != cudaSuccess)
+        return e;
     const dim3 grid(static_cast<unsigned>(a.max_splits), static_cast<unsigned>(a.num_kv_heads),
                     static_cast<unsigned>(a.batch));
-    // programmatic dependent launch: the grid may start while the previous
-    // kernel on the stream finishes; the kernel waits before its first read
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = T::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_split_kernel<kBf16, kPrecise>, k_map, v_map, a);
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = launch_config<kBf16, kPrecise, kCluster>(a, grid, stream, attr);
+    e = cudaLaunchKernelEx(&cfg, decode_split_kernel<kBf16, kPrecise, kCluster>, k_map, v_map, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+template <bool kCluster>
+cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                           cudaStream_t stream)
+{
+    if (a.bf16_cache)
+        return a.out_fp32 ? launch_split<true, true, kCluster>(a, k_map, v_map, stream)
+                          : launch_split<true, false, kCluster>(a, k_map, v_map, stream);
+    return a.out_fp32 ? launch_split<false, true, kCluster>(a, k_map, v_map, stream)
+                      : launch_split<false, false, kCluster>(a, k_map, v_map, stream);
+}
+
+template <bool kBf16>
+int cluster_capacity_query(int n)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || configure<kBf16, false, true>(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    DecodeArgs a = {};
+    a.max_splits = n;
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg =
+        launch_config<kBf16, false, true>(a, dim3(static_cast<unsigned>(n), 1, 1), nullptr, attr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_split_kernel<kBf16, false, true>, &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters;
 }
 
 } // namespace
@@ -663,11 +825,29 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
 {
     if (a.batch == 0)
         return cudaSuccess;
-    if (a.bf16_cache)
-        return a.out_fp32 ? launch_split<true, true>(a, k_map, v_map, stream)
-                          : launch_split<true, false>(a, k_map, v_map, stream);
-    return a.out_fp32 ? launch_split<false, true>(a, k_map, v_map, stream)
-                      : launch_split<false, false>(a, k_map, v_map, stream);
+    return a.cluster ? launch_variant<true>(a, k_map, v_map, stream)
+                     : launch_variant<false>(a, k_map, v_map, stream);
+}
+
+int decode_cluster_capacity(int n, bool bf16_cache)
+{
+    if (n < 2 || n > kMaxCluster)
+        return 0;
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, bool>, int> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(dev, n, bf16_cache);
+    auto it = cache.find(key);
+    if (it != cache.end())
+        return it->second;
+    const int c = bf16_cache ? cluster_capacity_query<true>(n) : cluster_capacity_query<false>(n);
+    cache[key] = c;
+    return c;
 }
 
 int decode_ctas_per_sm() { return kCtasPerSm; }

@@ -12,6 +12,7 @@ namespace kvq {
 constexpr int kHeadDim = 128;
 constexpr int kChunkTokens = 32;     // tokens one warp consumes per pipeline stage
 constexpr int kMaxGroup = 8;         // query heads per KV head on one mma n-tile
+constexpr int kMaxCluster = 8;       // splits merged inside one thread-block cluster
 
 struct AppendArgs {
     const void *k_new, *v_new;       // bf16 [T][Hkv][D]
@@ -70,6 +71,8 @@ struct DecodeArgs {
     float *ws_o;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, num_pages;
     int32_t max_pages_per_seq, split_tokens, max_splits;
+    int32_t cluster;                 // 0: combine through memory; else the splits of a
+                                     // (request, KV head) form one cluster of max_splits CTAs
     float qk_scale_log2;             // softmax_scale * log2(e)
     bool out_fp32, bf16_cache;
 };
@@ -80,6 +83,9 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                           cudaStream_t stream);
 int decode_ctas_per_sm();
+// How many clusters of n split CTAs can be resident at once on the current
+// device (0 if clusters of n cannot be used).
+int decode_cluster_capacity(int n, bool bf16_cache);
 
 // Box height (in 128-byte rows) of one bulk copy for a page size.
 inline int tma_box_rows(int page_size, bool bf16_cache)

@@ -196,6 +196,15 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tensor_m
         : "memory");
 }
 
+// Hint: bring one box of a 2-D tensor into L2 (no shared memory, no
+// barrier, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tensor_map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
@@ -221,6 +230,39 @@ __device__ __forceinline__ void grid_dependency_wait()
 __device__ __forceinline__ void grid_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------ thread-block clusters
+// Rank of this CTA within its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives
+// (release: its earlier shared-memory writes become visible to the cluster)
+// and waits for all the others (acquire).  Called by whole warps.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 } // namespace kvq

@@ -191,7 +191,10 @@ def _decode_case(w, cache_dtype, out_fp32, num_splits, abort=None):
 def test_decode_attention_matches_oracle(g, ps, cache, out_kind):
     w = W.make_custom(LENS, group=g, page_size=ps, seed=g * 100 + ps, outlier_frac=0.01)
     cd = kvq.KVQ_CACHE_FP8_E4M3 if cache == "fp8" else kvq.KVQ_CACHE_BF16
-    for splits in (0, 1, 5):
+    # 5 splits: small batches merge them through distributed shared memory
+    # (one cluster per request and KV head); 12 (> 8, the cluster limit):
+    # through the workspace
+    for splits in (0, 1, 5, 12):
         _, got, ref = _decode_case(w, cd, out_kind == "fp32", splits)
         assert_close(got, ref, out_kind, f"g{g} ps{ps} {cache} splits{splits}")
 
@@ -206,7 +209,7 @@ def test_decode_edge_requests_zeroed():
     abort[5] = 1
     rng = np.random.default_rng(4)
     finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
-    for splits in (1, 0, 4):
+    for splits in (1, 0, 4, 12):
         dw = DeviceWorkload(w, kvq.KVQ_CACHE_FP8_E4M3, populate=False)
         dw.k_cache.copy_(torch.from_numpy(rng.choice(finite, size=w.cache_shape()).astype(np.uint8)))
         dw.v_cache.copy_(torch.from_numpy(rng.choice(finite, size=w.cache_shape()).astype(np.uint8)))
@@ -218,6 +221,28 @@ def test_decode_edge_requests_zeroed():
         for r in (1, 2, 3, 4, 5):
             assert np.all(got[r] == 0.0), (splits, r)
         assert np.all(np.isfinite(got[0])) and np.any(got[0] != 0)
+
+
+def test_cluster_and_workspace_combine_agree():
+    """The two forms of the split combine give the same attention."""
+    w = W.make_custom([3000, 1, 700, 2049, 64], group=8, page_size=16, seed=21)
+    dw = DeviceWorkload(w)
+    dw.append()
+    counters = (w.batch * w.num_kv_heads * 4 + 255) // 256 * 256
+    _, n6, ws6 = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads, w.max_pages_per_seq, 6)
+    _, n12, ws12 = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads, w.max_pages_per_seq, 12)
+    assert n6 == 6 and ws6 == counters                      # 10 clusters of 6 CTAs: resident
+    assert n12 == 12 and ws12 > counters                    # partials go through the workspace
+    outs = []
+    for splits in (6, 12):
+        out = dw.out(True)
+        dw.attend(out, dw.workspace(splits), None, splits)
+        outs.append(out_to_np(out))
+    kc, vc = oracle_caches(dw)
+    ref = oracle_attention(dw, kc, vc)
+    for got in outs:
+        assert_close(got, ref, "fp32", "combine forms")
+    assert np.all(np.abs(outs[0] - outs[1]) <= 4e-4 + 4e-4 * np.abs(outs[1]))
 
 
 def test_decode_invariant_to_physical_page_placement():
