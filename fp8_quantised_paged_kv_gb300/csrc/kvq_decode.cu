@@ -45,7 +45,6 @@ constexpr int kCtasPerSm = 3;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // give up on a copy after ~1 s
-constexpr int kMaxSplits = 1024;
 constexpr int kPrefetchTokens = 256;             // per split, requested into L2 before the wait
 
 template <bool kBf16Cache>
@@ -97,10 +96,17 @@ __device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool 
 }
 
 
+// The warps' merge area holds one row of 128 floats per (warp, head).  Row
+// stride and a skew of 2 words per 32 dims make the fragment stores (a lane
+// writes dims 16*(lane/4) + 2i, +1 of heads 2*(lane%4), +1) hit 16 distinct
+// bank pairs per half-warp, and keep the row reads (thread d) conflict-free.
+constexpr int kMergeStride = 146;                 // >= 128 + 6, == 2 (mod 16)
+__device__ __forceinline__ int merge_col(int d) { return d + 2 * (d >> 5); }
+
 // Shared-memory offset (in floats) of the combine scratch: just past the
 // warps' merge area, inside the ring (idle by then).
 constexpr int kScratchOffset =
-    (kWarps * kMaxGroup * kHeadDim + 3 * kWarps * kMaxGroup + 2 * kMaxGroup + 3) / 4 * 4;
+    (kWarps * kMaxGroup * kMergeStride + 3 * kWarps * kMaxGroup + 2 * kMaxGroup + 3) / 4 * 4;
 static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kHeadDim) * 4 <= Tile<false>::kRingBytes,
               "combine scratch and cluster partial fit in the idle ring");
 
@@ -656,18 +662,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 
     // ---- merge the four warps' states in shared memory (ring is free now)
     float *sm_o = reinterpret_cast<float *>(smem);                     // [kWarps][8][128]
-    float *sm_m = sm_o + kWarps * kMaxGroup * kHeadDim;               // [kWarps][8]
+    float *sm_m = sm_o + kWarps * kMaxGroup * kMergeStride;           // [kWarps][8]
     float *sm_l = sm_m + kWarps * kMaxGroup;                          // [kWarps][8]
 #pragma unroll
     for (int j = 0; j < 2; ++j)
         l_run[j] = warp_sum_over_rows(l_run[j]);
     {
-        float *ow = sm_o + warp * kMaxGroup * kHeadDim;
+        float *ow = sm_o + warp * kMaxGroup * kMergeStride;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int d = 16 * gq + 2 * i;
-            *reinterpret_cast<float2 *>(ow + (2 * tq) * kHeadDim + d) = make_float2(o[i][0], o[i][2]);
-            *reinterpret_cast<float2 *>(ow + (2 * tq + 1) * kHeadDim + d) = make_float2(o[i][1], o[i][3]);
+            const int c = merge_col(16 * gq + 2 * i);
+            *reinterpret_cast<float2 *>(ow + (2 * tq) * kMergeStride + c) = make_float2(o[i][0], o[i][2]);
+            *reinterpret_cast<float2 *>(ow + (2 * tq + 1) * kMergeStride + c) = make_float2(o[i][1], o[i][3]);
         }
         if (gq == 0) {
             sm_m[warp * kMaxGroup + 2 * tq] = m_run[0];
@@ -704,7 +710,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
-            acc += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * sm_f[h * kWarps + w];
+            acc += sm_o[(w * kMaxGroup + h) * kMergeStride + merge_col(d)] * sm_f[h * kWarps + w];
         const float val = acc * sm_t[h];
         const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + hq0 + h;
         if constexpr (kCluster) {
