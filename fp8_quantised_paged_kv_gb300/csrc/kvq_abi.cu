@@ -112,7 +112,8 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (num_splits > 0) {
         want = num_splits;
     } else {
-        const int64_t slots = static_cast<int64_t>(sm_count()) * kvq::decode_ctas_per_sm();
+        const int64_t slots = static_cast<int64_t>(sm_count()) *
+                              kvq::decode_ctas_per_sm(d->cache_dtype == KVQ_CACHE_BF16);
         want = auto_splits(static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads, max_ctx, slots);
     }
     if (want < 1)

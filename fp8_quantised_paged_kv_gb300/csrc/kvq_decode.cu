@@ -27,6 +27,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -485,153 +486,162 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         const int64_t left = t1 - tok;
         const int n_valid = left < kChunkTokens ? static_cast<int>(left) : kChunkTokens;
 
-        // ---- S^T = K Q^T for the two 16-token m-tiles
-        float sc[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-            const int r0 = mt * 16 + gq, r1 = r0 + 8;
-            if constexpr (kBf16Cache) {
-                uint32_t w0[16], w1[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int line0 = 2 * r0 + (tq >> 1), line1 = 2 * r1 + (tq >> 1);
-                    const uint4 x0 = lds128(ks, swz(line0, (tq & 1) * 4 + j));
-                    const uint4 x1 = lds128(ks, swz(line1, (tq & 1) * 4 + j));
-                    w0[4 * j] = x0.x; w0[4 * j + 1] = x0.y; w0[4 * j + 2] = x0.z; w0[4 * j + 3] = x0.w;
-                    w1[4 * j] = x1.x; w1[4 * j + 1] = x1.y; w1[4 * j + 2] = x1.z; w1[4 * j + 3] = x1.w;
+        // The chunk's arithmetic; a full chunk (every token valid, the
+        // common case) is compiled without the masking of tail tokens.
+        auto chunk = [&](auto full) {
+            constexpr bool kFull = decltype(full)::value;
+            // ---- S^T = K Q^T for the two 16-token m-tiles
+            float sc[2][4];
+    #pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+                const int r0 = mt * 16 + gq, r1 = r0 + 8;
+                if constexpr (kBf16Cache) {
+                    uint32_t w0[16], w1[16];
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int line0 = 2 * r0 + (tq >> 1), line1 = 2 * r1 + (tq >> 1);
+                        const uint4 x0 = lds128(ks, swz(line0, (tq & 1) * 4 + j));
+                        const uint4 x1 = lds128(ks, swz(line1, (tq & 1) * 4 + j));
+                        w0[4 * j] = x0.x; w0[4 * j + 1] = x0.y; w0[4 * j + 2] = x0.z; w0[4 * j + 3] = x0.w;
+                        w1[4 * j] = x1.x; w1[4 * j + 1] = x1.y; w1[4 * j + 2] = x1.z; w1[4 * j + 3] = x1.w;
+                    }
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(sc[mt], w0[2 * kk], w1[2 * kk], w0[2 * kk + 1], w1[2 * kk + 1],
+                                 qf[kk][0], qf[kk][1]);
+                } else {
+                    const uint4 x0a = lds128(ks, swz(r0, 2 * tq)), x0b = lds128(ks, swz(r0, 2 * tq + 1));
+                    const uint4 x1a = lds128(ks, swz(r1, 2 * tq)), x1b = lds128(ks, swz(r1, 2 * tq + 1));
+                    const uint32_t w0[8] = {x0a.x, x0a.y, x0a.z, x0a.w, x0b.x, x0b.y, x0b.z, x0b.w};
+                    const uint32_t w1[8] = {x1a.x, x1a.y, x1a.z, x1a.w, x1b.x, x1b.y, x1b.z, x1b.w};
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16(sc[mt], lo16_e4m3x2_to_f16x2(w0[kk]), lo16_e4m3x2_to_f16x2(w1[kk]),
+                                hi16_e4m3x2_to_f16x2(w0[kk]), hi16_e4m3x2_to_f16x2(w1[kk]),
+                                qf[kk][0], qf[kk][1]);
                 }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(sc[mt], w0[2 * kk], w1[2 * kk], w0[2 * kk + 1], w1[2 * kk + 1],
-                             qf[kk][0], qf[kk][1]);
-            } else {
-                const uint4 x0a = lds128(ks, swz(r0, 2 * tq)), x0b = lds128(ks, swz(r0, 2 * tq + 1));
-                const uint4 x1a = lds128(ks, swz(r1, 2 * tq)), x1b = lds128(ks, swz(r1, 2 * tq + 1));
-                const uint32_t w0[8] = {x0a.x, x0a.y, x0a.z, x0a.w, x0b.x, x0b.y, x0b.z, x0b.w};
-                const uint32_t w1[8] = {x1a.x, x1a.y, x1a.z, x1a.w, x1b.x, x1b.y, x1b.z, x1b.w};
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_f16(sc[mt], lo16_e4m3x2_to_f16x2(w0[kk]), lo16_e4m3x2_to_f16x2(w1[kk]),
-                            hi16_e4m3x2_to_f16x2(w0[kk]), hi16_e4m3x2_to_f16x2(w1[kk]),
-                            qf[kk][0], qf[kk][1]);
             }
-        }
 
-        // ---- online softmax (log2 domain); lane holds heads 2tq, 2tq+1
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = mt * 16 + gq + ((i & 2) ? 8 : 0);
-                float x = sc[mt][i] * qk_scale;
-                x = row < n_valid ? x : -INFINITY;
-                sc[mt][i] = x;
-                mx[i & 1] = fmaxf(mx[i & 1], x);
+            // ---- online softmax (log2 domain); lane holds heads 2tq, 2tq+1
+            float mx[2] = {-INFINITY, -INFINITY};
+    #pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = mt * 16 + gq + ((i & 2) ? 8 : 0);
+                    float x = sc[mt][i] * qk_scale;
+                    x = (kFull || row < n_valid) ? x : -INFINITY;
+                    sc[mt][i] = x;
+                    mx[i & 1] = fmaxf(mx[i & 1], x);
+                }
             }
-        }
-        float alpha[2], base[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float mnew = fmaxf(m_run[j], warp_max_over_rows(mx[j]));
-            base[j] = mnew == -INFINITY ? 0.f : mnew;
-            alpha[j] = fast_exp2(m_run[j] - base[j]);
-            m_run[j] = mnew;
-        }
-        float psum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float p = fast_exp2(sc[mt][i] - base[i & 1]);
-                sc[mt][i] = p;
-                psum[i & 1] += p;
+            float alpha[2], base[2];
+    #pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float mnew = fmaxf(m_run[j], warp_max_over_rows(mx[j]));
+                base[j] = mnew == -INFINITY ? 0.f : mnew;
+                alpha[j] = fast_exp2(m_run[j] - base[j]);
+                m_run[j] = mnew;
             }
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-            l_run[j] = l_run[j] * alpha[j] + psum[j];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            o[i][0] *= alpha[0];
-            o[i][1] *= alpha[1];
-            o[i][2] *= alpha[0];
-            o[i][3] *= alpha[1];
-        }
+            float psum[2] = {0.f, 0.f};
+    #pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float p = fast_exp2(sc[mt][i] - base[i & 1]);
+                    sc[mt][i] = p;
+                    psum[i & 1] += p;
+                }
+            }
+    #pragma unroll
+            for (int j = 0; j < 2; ++j)
+                l_run[j] = l_run[j] * alpha[j] + psum[j];
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i][0] *= alpha[0];
+                o[i][1] *= alpha[1];
+                o[i][2] *= alpha[0];
+                o[i][3] *= alpha[1];
+            }
 
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            uint32_t x0, x1;
-            if constexpr (kBf16Cache) {
-                x0 = f32x2_to_bf16x2(sc[mt][0], sc[mt][1]);
-                x1 = f32x2_to_bf16x2(sc[mt][2], sc[mt][3]);
-            } else {
-                x0 = f32x2_to_f16x2(sc[mt][0], sc[mt][1]);
-                x1 = f32x2_to_f16x2(sc[mt][2], sc[mt][3]);
+            // ---- O^T += V^T P^T
+    #pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                uint32_t x0, x1;
+                if constexpr (kBf16Cache) {
+                    x0 = f32x2_to_bf16x2(sc[mt][0], sc[mt][1]);
+                    x1 = f32x2_to_bf16x2(sc[mt][2], sc[mt][3]);
+                } else {
+                    x0 = f32x2_to_f16x2(sc[mt][0], sc[mt][1]);
+                    x1 = f32x2_to_f16x2(sc[mt][2], sc[mt][3]);
+                }
+                const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
+                uint32_t pl0 = 0, pl1 = 0;
+                if constexpr (kPreciseP) {
+                    // second term carries what the 16-bit rounding of P dropped
+                    const float2 h0 = kBf16Cache ? bf16x2_to_f32x2(x0) : f16x2_to_f32x2(x0);
+                    const float2 h1 = kBf16Cache ? bf16x2_to_f32x2(x1) : f16x2_to_f32x2(x1);
+                    const uint32_t y0 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y)
+                                                   : f32x2_to_f16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y);
+                    const uint32_t y1 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y)
+                                                   : f32x2_to_f16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y);
+                    pl0 = movmatrix_trans(y0);
+                    pl1 = movmatrix_trans(y1);
+                }
+                // V rows of token slots 2tq, 2tq+1, 2tq+8, 2tq+9 of this m-tile
+                const int rv = mt * 16 + 2 * tq;
+                const int rows[4] = {rv, rv + 1, rv + 8, rv + 9};
+                if constexpr (kBf16Cache) {
+                    uint32_t R[4][8];
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int line = 2 * rows[q] + (gq >> 2);
+                        const uint4 lo = lds128(vs, swz(line, (gq & 3) * 2));
+                        const uint4 hi = lds128(vs, swz(line, (gq & 3) * 2 + 1));
+                        const bool keep = kFull || rows[q] < n_valid;
+                        R[q][0] = keep ? lo.x : 0u; R[q][1] = keep ? lo.y : 0u;
+                        R[q][2] = keep ? lo.z : 0u; R[q][3] = keep ? lo.w : 0u;
+                        R[q][4] = keep ? hi.x : 0u; R[q][5] = keep ? hi.y : 0u;
+                        R[q][6] = keep ? hi.z : 0u; R[q][7] = keep ? hi.w : 0u;
+                    }
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t a0 = prmt(R[0][i], R[1][i], 0x5410);
+                        const uint32_t a1 = prmt(R[0][i], R[1][i], 0x7632);
+                        const uint32_t a2 = prmt(R[2][i], R[3][i], 0x5410);
+                        const uint32_t a3 = prmt(R[2][i], R[3][i], 0x7632);
+                        mma_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
+                        if constexpr (kPreciseP)
+                            mma_bf16(o[i], a0, a1, a2, a3, pl0, pl1);
+                    }
+                } else {
+                    uint32_t R[4][4];
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = lds128(vs, swz(rows[q], gq));
+                        const bool keep = kFull || rows[q] < n_valid;
+                        R[q][0] = keep ? v.x : 0u; R[q][1] = keep ? v.y : 0u;
+                        R[q][2] = keep ? v.z : 0u; R[q][3] = keep ? v.w : 0u;
+                    }
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                        const uint32_t p01 = prmt(R[0][i >> 1], R[1][i >> 1], sel);
+                        const uint32_t p23 = prmt(R[2][i >> 1], R[3][i >> 1], sel);
+                        const uint32_t a0 = lo16_e4m3x2_to_f16x2(p01), a1 = hi16_e4m3x2_to_f16x2(p01);
+                        const uint32_t a2 = lo16_e4m3x2_to_f16x2(p23), a3 = hi16_e4m3x2_to_f16x2(p23);
+                        mma_f16(o[i], a0, a1, a2, a3, pb0, pb1);
+                        if constexpr (kPreciseP)
+                            mma_f16(o[i], a0, a1, a2, a3, pl0, pl1);
+                    }
+                }
             }
-            const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
-            uint32_t pl0 = 0, pl1 = 0;
-            if constexpr (kPreciseP) {
-                // second term carries what the 16-bit rounding of P dropped
-                const float2 h0 = kBf16Cache ? bf16x2_to_f32x2(x0) : f16x2_to_f32x2(x0);
-                const float2 h1 = kBf16Cache ? bf16x2_to_f32x2(x1) : f16x2_to_f32x2(x1);
-                const uint32_t y0 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y)
-                                               : f32x2_to_f16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y);
-                const uint32_t y1 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y)
-                                               : f32x2_to_f16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y);
-                pl0 = movmatrix_trans(y0);
-                pl1 = movmatrix_trans(y1);
-            }
-            // V rows of token slots 2tq, 2tq+1, 2tq+8, 2tq+9 of this m-tile
-            const int rv = mt * 16 + 2 * tq;
-            const int rows[4] = {rv, rv + 1, rv + 8, rv + 9};
-            if constexpr (kBf16Cache) {
-                uint32_t R[4][8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int line = 2 * rows[q] + (gq >> 2);
-                    const uint4 lo = lds128(vs, swz(line, (gq & 3) * 2));
-                    const uint4 hi = lds128(vs, swz(line, (gq & 3) * 2 + 1));
-                    const bool keep = rows[q] < n_valid;
-                    R[q][0] = keep ? lo.x : 0u; R[q][1] = keep ? lo.y : 0u;
-                    R[q][2] = keep ? lo.z : 0u; R[q][3] = keep ? lo.w : 0u;
-                    R[q][4] = keep ? hi.x : 0u; R[q][5] = keep ? hi.y : 0u;
-                    R[q][6] = keep ? hi.z : 0u; R[q][7] = keep ? hi.w : 0u;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t a0 = prmt(R[0][i], R[1][i], 0x5410);
-                    const uint32_t a1 = prmt(R[0][i], R[1][i], 0x7632);
-                    const uint32_t a2 = prmt(R[2][i], R[3][i], 0x5410);
-                    const uint32_t a3 = prmt(R[2][i], R[3][i], 0x7632);
-                    mma_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
-                    if constexpr (kPreciseP)
-                        mma_bf16(o[i], a0, a1, a2, a3, pl0, pl1);
-                }
-            } else {
-                uint32_t R[4][4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 v = lds128(vs, swz(rows[q], gq));
-                    const bool keep = rows[q] < n_valid;
-                    R[q][0] = keep ? v.x : 0u; R[q][1] = keep ? v.y : 0u;
-                    R[q][2] = keep ? v.z : 0u; R[q][3] = keep ? v.w : 0u;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-                    const uint32_t p01 = prmt(R[0][i >> 1], R[1][i >> 1], sel);
-                    const uint32_t p23 = prmt(R[2][i >> 1], R[3][i >> 1], sel);
-                    const uint32_t a0 = lo16_e4m3x2_to_f16x2(p01), a1 = hi16_e4m3x2_to_f16x2(p01);
-                    const uint32_t a2 = lo16_e4m3x2_to_f16x2(p23), a3 = hi16_e4m3x2_to_f16x2(p23);
-                    mma_f16(o[i], a0, a1, a2, a3, pb0, pb1);
-                    if constexpr (kPreciseP)
-                        mma_f16(o[i], a0, a1, a2, a3, pl0, pl1);
-                }
-            }
-        }
+        };
+        if (n_valid == kChunkTokens)
+            chunk(std::true_type{});
+        else
+            chunk(std::false_type{});
 
         // ---- refill this stage with the chunk kStages ahead
         __syncwarp();
@@ -856,7 +866,38 @@ int decode_cluster_capacity(int n, bool bf16_cache)
     return c;
 }
 
-int decode_ctas_per_sm() { return kCtasPerSm; }
+int decode_ctas_per_sm(bool bf16_cache)
+{
+    // resident CTAs per SM as the shared-memory footprint allows (no device)
+    const int by_smem = bf16_cache ? 233472 / (Tile<true>::kSmemBytes + 1024)
+                                   : 233472 / (Tile<false>::kSmemBytes + 1024);
+    const int fallback = by_smem < kCtasPerSm ? (by_smem > 0 ? by_smem : 1) : kCtasPerSm;
+    static std::mutex mu;
+    static std::map<std::pair<int, bool>, int> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fallback;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(dev, bf16_cache);
+    auto it = cache.find(key);
+    if (it != cache.end())
+        return it->second;
+    int n = 0;
+    cudaError_t e = bf16_cache ? configure<true, false, false>(dev) : configure<false, false, false>(dev);
+    if (e == cudaSuccess)
+        e = bf16_cache ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                             &n, decode_split_kernel<true, false, false>, kThreads, Tile<true>::kSmemBytes)
+                       : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                             &n, decode_split_kernel<false, false, false>, kThreads, Tile<false>::kSmemBytes);
+    if (e != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = fallback;
+    }
+    cache[key] = n;
+    return n;
+}
 
 cudaError_t read_device_error(uint32_t *bits, bool clear)
 {

@@ -82,7 +82,8 @@ struct DecodeArgs {
 // swizzle.
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                           cudaStream_t stream);
-int decode_ctas_per_sm();
+// Resident decode CTAs per SM for the cache type (occupancy of the kernel).
+int decode_ctas_per_sm(bool bf16_cache);
 // How many clusters of n split CTAs can be resident at once on the current
 // device (0 if clusters of n cannot be used).
 int decode_cluster_capacity(int n, bool bf16_cache);
