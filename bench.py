@@ -429,10 +429,11 @@ def run_churn(args):
     """32-layer churn workload: per step one tag check, then for every layer
     the append of each request's new token and the decode attention.  Reports
     the KV bytes the step reads per second and the tag check's share of the
-    step time (the pages' integrity-check overhead figure)."""
+    step time (the pages' integrity-check overhead figure).  With --graph the
+    65 launches of a step are captured once as a CUDA graph and replayed."""
     import torch
     import fp8_quantised_paged_kv_gb300 as kvq
-    from kvq_churn import ChurnDevice, ChurnState
+    from kvq_churn import ChurnDevice, ChurnGraphStep, ChurnState
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -440,26 +441,30 @@ def run_churn(args):
     kvq.kvq_device_error(clear=True)
     st = ChurnState(seed=rank)
     dev = ChurnDevice(st, layers=32, device=f"cuda:{local}", log_layers=())
+    gs = ChurnGraphStep(dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
+    if args.graph:
+        gs.load()
+        gs.capture()                     # consumes no step: the tables are reloaded below
     rows = []
     for i in range(args.warmup + args.steps):
-        bt, exp, seq, stale = st.tables()
-        bt_d, exp_d, seq_d, tags_d, slots, slots_d = dev.upload(bt, exp, seq)
-        vals = [dev.step_values(l, st.step_index) for l in range(dev.layers)]
-        outs = [torch.empty((st.batch, dev.hq, dev.D), dtype=torch.bfloat16, device=dev.device)
-                for _ in range(dev.layers)]
+        bt, exp, seq, stale, slots = gs.load()
         flush.zero_()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record(stream)
-        kvq.kvq_tag_check(bt_d, exp_d, seq_d, st.ps, tags_d, dev.abort)
-        e[1].record(stream)
-        for l in range(dev.layers):
-            q, kn, vn = vals[l]
-            kvq.kvq_append(dev.desc, kn, vn, slots_d, dev.k_scale[l], dev.v_scale[l], dev.abort,
-                           dev.k[l], dev.v[l])
-            kvq.kvq_decode_attn(dev.desc, q, dev.k[l], dev.v[l], dev.k_scale[l], dev.v_scale[l],
-                                bt_d, seq_d, dev.sigma, dev.abort, outs[l], dev.ws)
+        if args.graph:
+            gs.replay()
+            e[1].record(stream)
+        else:
+            dev.kvq.kvq_tag_check(gs.bt, gs.exp, gs.seq, st.ps, gs.tags, dev.abort)
+            e[1].record(stream)
+            for l in range(dev.layers):
+                kvq.kvq_append(dev.desc, gs.kn[l], gs.vn[l], gs.slots, dev.k_scale[l], dev.v_scale[l],
+                               dev.abort, dev.k[l], dev.v[l])
+                kvq.kvq_decode_attn(dev.desc, gs.q[l], dev.k[l], dev.v[l], dev.k_scale[l],
+                                    dev.v_scale[l], gs.bt, gs.seq, dev.sigma, dev.abort, gs.out[l],
+                                    dev.ws)
         e[2].record(stream)
         abort = dev.abort.cpu().numpy()
         live = (seq > 0) & (abort == 0)
@@ -482,10 +487,12 @@ def run_churn(args):
             "config": {"workload": "churn", "layers": 32, "batch": st.batch, "num_q_heads": dev.hq,
                        "num_kv_heads": dev.hkv, "page_size": st.ps,
                        "l2": "flushed before every timed step (512 MiB write)",
-                       "step": "tag check once, then 32 x (append + decode attention)"},
+                       "step": "tag check once, then 32 x (append + decode attention)",
+                       "launch": "one CUDA graph replay" if args.graph else "65 launches"},
             "tokens_per_s": round(float(reqs.sum() / (step.sum() / 1e3)), 1),
-            "tag_check_us": round(float(tag.mean() * 1e3), 2),
-            "tag_check_share_of_step": round(float(tag.sum() / step.sum()), 6),
+            "tag_check_us": None if args.graph else round(float(tag.mean() * 1e3), 2),
+            "tag_check_share_of_step": None if args.graph else round(float(tag.sum() / step.sum()), 6),
+            "gpu_launches": 65 * args.steps,
             "device_error_bits": kvq.kvq_device_error(),
         }))
     return 0
@@ -501,6 +508,7 @@ def main():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="churn: replay the step as a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

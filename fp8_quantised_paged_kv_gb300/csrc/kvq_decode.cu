@@ -228,15 +228,14 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2 };
 // have read it.  Every CTA of the cluster calls this exactly once.
 __device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part)
 {
-    static_assert(kThreads == kHeadDim, "one thread per output dimension");
     if (status != kPartialOk && threadIdx.x < kMaxGroup)
         part[threadIdx.x] = status == kPartialEmpty ? -INFINITY : __int_as_float(0x7FC00000);
     cluster_sync();
     const int g = a.group, n = a.max_splits;
     const int rank = static_cast<int>(cluster_ctarank());
     const uint32_t base = smem_addr(part);
-    const int d = threadIdx.x;
-    for (int h = rank; h < g; h += n) {
+    for (int h = rank; h < g; h += n)
+    for (int d = threadIdx.x; d < kHeadDim; d += kThreads) {
         float lse[kMaxCluster], ov[kMaxCluster];
 #pragma unroll
         for (int s = 0; s < kMaxCluster; ++s) {
@@ -577,7 +576,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     x1 = f32x2_to_f16x2(sc[mt][2], sc[mt][3]);
                 }
                 const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
-                uint32_t pl0 = 0, pl1 = 0;
+                [[maybe_unused]] uint32_t pl0 = 0, pl1 = 0;
                 if constexpr (kPreciseP) {
                     // second term carries what the 16-bit rounding of P dropped
                     const float2 h0 = kBf16Cache ? bf16x2_to_f32x2(x0) : f16x2_to_f32x2(x0);

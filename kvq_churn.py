@@ -294,3 +294,71 @@ class ChurnDevice:
                 if hit is not None:
                     k[i * ps + o], v[i * ps + o] = hit
         return k[:length], v[:length]
+
+
+class ChurnGraphStep:
+    """The churn step (one tag check, then append + decode attention for every
+    layer) over fixed device buffers, so that it can be captured once as a
+    CUDA graph and replayed each step after the step's tables and values are
+    copied in."""
+
+    def __init__(self, dev: ChurnDevice):
+        torch = dev.torch
+        self.dev, s = dev, dev.s
+        B, maxp, d = s.batch, s.max_pages, dev.device
+        self.bt = torch.empty((B, maxp), dtype=torch.int32, device=d)
+        self.exp = torch.empty((B, maxp), dtype=torch.int32, device=d)
+        self.seq = torch.empty(B, dtype=torch.int32, device=d)
+        self.tags = torch.empty(s.num_pages, dtype=torch.int32, device=d)
+        self.slots = torch.empty(B, dtype=torch.int64, device=d)
+        shape_q, shape_kv = (B, dev.hq, dev.D), (B, dev.hkv, dev.D)
+        self.q = [torch.empty(shape_q, dtype=torch.bfloat16, device=d) for _ in range(dev.layers)]
+        self.kn = [torch.empty(shape_kv, dtype=torch.bfloat16, device=d) for _ in range(dev.layers)]
+        self.vn = [torch.empty(shape_kv, dtype=torch.bfloat16, device=d) for _ in range(dev.layers)]
+        self.out = [torch.empty(shape_q, dtype=torch.bfloat16, device=d) for _ in range(dev.layers)]
+        self.graph = None
+
+    def load(self):
+        """Copy this step's tables and per-layer values into the fixed buffers.
+        Returns (bt, exp, seq, stale, slots) on the host."""
+        dev, s = self.dev, self.dev.s
+        bt, exp, seq, stale = s.tables()
+        bt_d, exp_d, seq_d, tags_d, slots, slots_d = dev.upload(bt, exp, seq)
+        self.bt.copy_(bt_d)
+        self.exp.copy_(exp_d)
+        self.seq.copy_(seq_d)
+        self.tags.copy_(tags_d)
+        self.slots.copy_(slots_d)
+        for l in range(dev.layers):
+            q, kn, vn = dev.step_values(l, s.step_index)
+            self.q[l].copy_(q)
+            self.kn[l].copy_(kn)
+            self.vn[l].copy_(vn)
+        return bt, exp, seq, stale, slots
+
+    def launch(self, stream=None):
+        dev, kvq, s = self.dev, self.dev.kvq, self.dev.s
+        kvq.kvq_tag_check(self.bt, self.exp, self.seq, s.ps, self.tags, dev.abort, stream)
+        for l in range(dev.layers):
+            kvq.kvq_append(dev.desc, self.kn[l], self.vn[l], self.slots, dev.k_scale[l], dev.v_scale[l],
+                           dev.abort, dev.k[l], dev.v[l], stream)
+            kvq.kvq_decode_attn(dev.desc, self.q[l], dev.k[l], dev.v[l], dev.k_scale[l], dev.v_scale[l],
+                                self.bt, self.seq, dev.sigma, dev.abort, self.out[l], dev.ws, 0, stream)
+
+    def capture(self):
+        """Capture launch() as a CUDA graph (after one eager launch has run
+        every first-call setup of the library)."""
+        torch = self.dev.torch
+        side = torch.cuda.Stream(device=self.dev.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.launch(side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.launch(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
