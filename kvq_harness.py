@@ -137,6 +137,30 @@ class DeviceWorkload:
         return self.attend(out, workspace, self.abort, num_splits, stream)
 
     # ---------------------------------------------------------- oracle feed
+    STEP_INPUTS = ("q", "k_new", "v_new", "append_slots", "block_table", "seq_lens", "expected_tags")
+
+    def pack_step_inputs(self):
+        """Move the step's inputs into one device buffer (256-byte aligned
+        segments) and return it with a pinned host copy, so that a host-fed
+        step is a single host-to-device copy.  The workload's tensors become
+        views of the device buffer."""
+        import torch
+        offs, total = [], 0
+        for n in self.STEP_INPUTS:
+            t = getattr(self, n)
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        dev = torch.zeros(total, dtype=torch.uint8, device=self.device)
+        host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        for n, o in zip(self.STEP_INPUTS, offs):
+            t = getattr(self, n)
+            nb = t.numel() * t.element_size()
+            view = dev[o:o + nb].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            host[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+            setattr(self, n, view)
+        return host, dev
+
     def host_request(self, r: int):
         """bf16 bits (numpy uint16) of request r: K and V of all L tokens in
         logical order [L][Hkv][D], and q [Hq][D] -- regenerated from the seed."""

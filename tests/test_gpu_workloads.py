@@ -105,3 +105,20 @@ def test_split_counts_agree_at_full_size():
         torch.cuda.synchronize()
         a, b = out_to_np(out), out_to_np(o2)
         assert np.all(np.abs(a - b) <= 4e-4 + 4e-4 * np.abs(a))
+
+
+def test_packed_step_inputs_give_the_same_step():
+    """The host-fed step keeps its inputs in one packed buffer (one copy per
+    step); running the step on those views changes nothing."""
+    w = W.make("uniform8", scale_down=8)
+    dw = DeviceWorkload(w)
+    out1 = dw.out(False)
+    dw.step(out1, dw.workspace(0))
+    host, dev = dw.pack_step_inputs()
+    assert host.numel() == dev.numel() and host.numel() % 256 == 0
+    dev.zero_()
+    dev.copy_(host.to(dev.device))
+    out2 = dw.out(False)
+    dw.step(out2, dw.workspace(0))
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
