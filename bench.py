@@ -265,12 +265,21 @@ def run_ours(args):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        dw.tag_check_append(stream)            # batched tag check + FP8 append, one launch
+        if args.fused_append:
+            dw.tag_check(stream)               # batched tag check
+        else:
+            dw.tag_check_append(stream)        # batched tag check + FP8 append, one launch
         if ev is not None:
             ev[1].record(stream)
-        kvq.kvq_decode_attn(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
-                            dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out, ws,
-                            args.num_splits, stream)
+        if args.fused_append:                  # append of the new token inside the decode launch
+            kvq.kvq_decode_attn_append(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale,
+                                       dw.v_scale, dw.block_table, dw.seq_lens, w.softmax_scale,
+                                       dw.abort, dw.k_new, dw.v_new, out, ws, args.num_splits,
+                                       stream)
+        else:
+            kvq.kvq_decode_attn(dw.desc, dw.q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
+                                dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out, ws,
+                                args.num_splits, stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -392,12 +401,17 @@ def run_ours(args):
                        "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3",
                        "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
                        "split_combine": combine,
+                       "step": ("kvq_tag_check, then kvq_decode_attn_append" if args.fused_append
+                                else "kvq_tag_check_append, then kvq_decode_attn"),
                        "l2": "flushed before every timed step (512 MiB write)",
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": round(agg["tokens_per_s"], 1),
             "hbm_frac_of_measured": round(kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
-            "kernel_us": {"tag_check_append": round(pre_ms * 1e3, 2),
-                          "decode_attn (split + fused combine)": round(attn_ms * 1e3, 2)},
+            "kernel_us": ({"tag_check": round(pre_ms * 1e3, 2),
+                           "decode_attn_append (append + split + fused combine)": round(attn_ms * 1e3, 2)}
+                          if args.fused_append else
+                          {"tag_check_append": round(pre_ms * 1e3, 2),
+                           "decode_attn (split + fused combine)": round(attn_ms * 1e3, 2)}),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": "decode_split_kernel", "peak_kind": peak_kind,
@@ -435,7 +449,7 @@ def run_churn(args):
     kvq.kvq_device_error(clear=True)
     st = ChurnState(seed=rank)
     dev = ChurnDevice(st, layers=32, device=f"cuda:{local}", log_layers=())
-    gs = ChurnGraphStep(dev)
+    gs = ChurnGraphStep(dev, fused_append=args.fused_append)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
     if args.graph:
@@ -450,6 +464,13 @@ def run_churn(args):
         if args.graph:
             gs.replay()
             e[1].record(stream)
+        elif args.fused_append:
+            kvq.kvq_tag_check(gs.bt, gs.exp, gs.seq, st.ps, gs.tags, dev.abort)
+            e[1].record(stream)
+            for l in range(dev.layers):
+                kvq.kvq_decode_attn_append(dev.desc, gs.q[l], dev.k[l], dev.v[l], dev.k_scale[l],
+                                           dev.v_scale[l], gs.bt, gs.seq, dev.sigma, dev.abort,
+                                           gs.kn[l], gs.vn[l], gs.out[l], dev.ws)
         else:
             dev.kvq.kvq_tag_check(gs.bt, gs.exp, gs.seq, st.ps, gs.tags, dev.abort)
             e[1].record(stream)
@@ -482,11 +503,14 @@ def run_churn(args):
                        "num_kv_heads": dev.hkv, "page_size": st.ps,
                        "l2": "flushed before every timed step (512 MiB write)",
                        "step": "tag check once, then 32 x (append + decode attention)",
-                       "launch": "one CUDA graph replay" if args.graph else "65 launches"},
+                       "launch": ("one CUDA graph replay" if args.graph else
+                                  "33 launches" if args.fused_append else "65 launches"),
+                       "append": ("inside each layer's decode launch" if args.fused_append
+                                  else "its own launch per layer")},
             "tokens_per_s": round(float(reqs.sum() / (step.sum() / 1e3)), 1),
             "tag_check_us": None if args.graph else round(float(tag.mean() * 1e3), 2),
             "tag_check_share_of_step": None if args.graph else round(float(tag.sum() / step.sum()), 6),
-            "gpu_launches": 65 * args.steps,
+            "gpu_launches": (33 if args.fused_append else 65) * args.steps,
             "device_error_bits": kvq.kvq_device_error(),
         }))
     return 0
@@ -503,6 +527,8 @@ def main():
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="churn: replay the step as a CUDA graph")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="step = tag check, then decode attention with the append fused in")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

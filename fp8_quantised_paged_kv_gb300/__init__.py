@@ -61,6 +61,8 @@ _SIGS = {
     "kvq_decode_plan": ["desc", "i32", "i32", "i32", "i32", "p", "p", "p"],
     "kvq_decode_attn": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
                         "p", "p", "i32", "p", "size", "i32", "p"],
+    "kvq_decode_attn_append": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
+                               "p", "p", "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
     "kvq_amax_scales": ["desc", "p", "p", "p", "i32", "p", "p", "p"],
     "kvq_quantize_pages": ["desc", "p", "p", "p", "desc", "p", "p", "p", "i32", "p", "p", "p"],
@@ -249,6 +251,34 @@ def kvq_decode_attn(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, se
     """Paged decode attention into ``out`` (bf16 or fp32 [B][Hq][D])."""
     return _decode("kvq_decode_attn", desc, q, k_cache, v_cache, k_scale, v_scale, block_table,
                    seq_lens, softmax_scale, abort_flags, out, workspace, num_splits, stream)
+
+
+def kvq_decode_attn_append(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                           softmax_scale, abort_flags, k_new, v_new, out, workspace, num_splits=0,
+                           stream=None):
+    """Append request r's new token (row r of k_new/v_new, bf16 [B][Hkv][D]) at
+    its position seq_lens[r] - 1, then paged decode attention into ``out``:
+    one launch, the same results as kvq_append followed by kvq_decode_attn."""
+    import torch
+    B, Hq, D = q.shape
+    _expect(q, torch.bfloat16, (B, Hq, desc.head_dim), "q")
+    _expect(block_table, torch.int32, None, "block_table")
+    _expect(seq_lens, torch.int32, (B,), "seq_lens")
+    _expect(k_new, torch.bfloat16, (B, desc.num_kv_heads, desc.head_dim), "k_new")
+    _expect(v_new, torch.bfloat16, (B, desc.num_kv_heads, desc.head_dim), "v_new")
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("out: expected bf16 or fp32 [B][Hq][D]")
+    out_dtype = KVQ_OUT_FP32 if out.dtype == torch.float32 else KVQ_OUT_BF16
+    if abort_flags is not None:
+        _expect(abort_flags, torch.uint8, (B,), "abort_flags")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kvq_decode_attn_append(
+        ctypes.byref(desc.c()), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        ctypes.c_float(softmax_scale), _ptr(abort_flags), _ptr(k_new), _ptr(v_new), _ptr(out),
+        out_dtype, _ptr(workspace), ws_bytes, num_splits, _stream(stream))
+    _check("kvq_decode_attn_append", st)
+    return out
 
 
 def kvq_device_error(clear: bool = False) -> int:

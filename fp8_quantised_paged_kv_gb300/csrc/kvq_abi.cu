@@ -241,6 +241,7 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     if (!aligned16(workspace))
         return KVQ_ERR_INVALID_ARG;
     kvq::DecodeArgs &a = call->args;
+    a = kvq::DecodeArgs{};
     a.q = q;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
@@ -494,6 +495,34 @@ kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t ba
                                    num_splits, &call);
     if (st != KVQ_OK || batch == 0)
         return st;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
+        return KVQ_ERR_CUDA;
+    return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                  int32_t num_q_heads, void *k_cache, void *v_cache,
+                                  const float *k_scale, const float *v_scale,
+                                  const int32_t *block_table, int32_t max_pages_per_seq,
+                                  const int32_t *seq_lens, float softmax_scale,
+                                  const uint8_t *abort_flags, const void *k_new, const void *v_new,
+                                  void *out, int32_t out_dtype, void *workspace,
+                                  size_t workspace_bytes, int32_t num_splits, kvq_stream_t stream)
+{
+    DecodeCall call;
+    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
+                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
+                                   num_splits, &call);
+    if (st != KVQ_OK || batch == 0)
+        return st;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return KVQ_ERR_INVALID_ARG;
+    call.args.k_new = k_new;
+    call.args.v_new = v_new;
+    call.args.k_cache = k_cache;
+    call.args.v_cache = v_cache;
     CUtensorMap km, vm;
     if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
         return KVQ_ERR_CUDA;

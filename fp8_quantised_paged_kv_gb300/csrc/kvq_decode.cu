@@ -33,6 +33,7 @@
 
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
+#include "kvq_rowops.cuh"
 
 namespace kvq {
 
@@ -376,6 +377,39 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         fence_mbar_init();
     }
     bad = __syncthreads_or(bad);
+
+    // Fused append (kvq_decode_attn_append): the split holding token len - 1
+    // writes that token's codes for KV head kvh into the cache now (when its
+    // page id is valid, as kvq_append would) and patches them into its tile
+    // when the chunk's copy lands, so its own attention uses them without
+    // reading them back.
+    int it_new = -1;
+    using NewRow = std::conditional_t<kBf16Cache, uint2, uint32_t>;   // a lane's part of the row
+    NewRow new_k{}, new_v{};
+    if (a.k_new != nullptr && split == nsplit - 1) {
+        const int64_t tpos = len - 1;
+        const int c_last = static_cast<int>((tpos - t0) / kChunkTokens);
+        const int32_t page = page_list[static_cast<int>(tpos / ps) - first_page];
+        if (warp == c_last % kWarps && page >= 0 && page < a.num_pages) {
+            it_new = c_last / kWarps;
+            const int64_t src = (static_cast<int64_t>(b) * a.num_kv_heads + kvh) * kHeadDim + 4 * lane;
+            const uint2 xk = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.k_new) + src);
+            const uint2 xv = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.v_new) + src);
+            const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + tpos % ps;
+            if constexpr (kBf16Cache) {
+                new_k = xk;
+                new_v = xv;
+                *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.k_cache) + row * 256 + 8 * lane) = xk;
+                *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.v_cache) + row * 256 + 8 * lane) = xv;
+            } else {
+                new_k = encode4_e4m3(xk.x, xk.y, a.k_scale[kvh]);
+                new_v = encode4_e4m3(xv.x, xv.y, a.v_scale[kvh]);
+                *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.k_cache) + row * 128 + 4 * lane) = new_k;
+                *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.v_cache) + row * 128 + 4 * lane) = new_v;
+            }
+        }
+    }
+
     if (bad) {
         if constexpr (kCluster)
             cluster_finish(a, b, kvh, kPartialInvalid, part);
@@ -482,6 +516,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         const uint8_t *vs = ks + T::kBytes;
         const int c = warp + it * kWarps;
         const int64_t tok = t0 + static_cast<int64_t>(c) * kChunkTokens;
+        if (it == it_new) {                  // fused append: the new token's row
+            const int r = static_cast<int>(len - 1 - tok);
+            uint8_t *kt = ring + st * T::kStageBytes;
+            uint8_t *vt = kt + T::kBytes;
+            if constexpr (kBf16Cache) {
+                const uint32_t off = swz(2 * r + (lane >> 4), (lane & 15) >> 1) + 8 * (lane & 1);
+                *reinterpret_cast<uint2 *>(kt + off) = new_k;
+                *reinterpret_cast<uint2 *>(vt + off) = new_v;
+            } else {
+                const uint32_t off = swz(r, lane >> 2) + 4 * (lane & 3);
+                *reinterpret_cast<uint32_t *>(kt + off) = new_k;
+                *reinterpret_cast<uint32_t *>(vt + off) = new_v;
+            }
+            __syncwarp();
+        }
         const int64_t left = t1 - tok;
         const int n_valid = left < kChunkTokens ? static_cast<int>(left) : kChunkTokens;
 

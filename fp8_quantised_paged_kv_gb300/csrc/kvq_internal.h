@@ -71,6 +71,8 @@ struct DecodeArgs {
     float *ws_o;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, num_pages;
     int32_t max_pages_per_seq, split_tokens, max_splits;
+    const void *k_new, *v_new;       // fused append: bf16 [B][Hkv][D] new token, else null
+    void *k_cache, *v_cache;         // fused append: the caches the token is written to
     int32_t cluster;                 // 0: combine through memory; else the splits of a
                                      // (request, KV head) form one cluster of max_splits CTAs
     float qk_scale_log2;             // softmax_scale * log2(e)

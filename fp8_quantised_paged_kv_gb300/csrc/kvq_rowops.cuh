@@ -56,6 +56,18 @@ __device__ __forceinline__ bool tag_check_request(const int32_t *block_table,
     return __syncthreads_or(bad) != 0;
 }
 
+// Four bf16 elements (two words) -> four e4m3 codes e4m3(x / scale), one
+// IEEE fp32 division each, rounding to nearest even, saturating at +-448;
+// element 0 in the low byte.
+__device__ __forceinline__ uint32_t encode4_e4m3(uint32_t w0, uint32_t w1, float scale)
+{
+    const float2 p0 = bf16x2_to_f32x2(w0);
+    const float2 p1 = bf16x2_to_f32x2(w1);
+    const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(p0.x, scale), __fdiv_rn(p0.y, scale));
+    const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(p1.x, scale), __fdiv_rn(p1.y, scale));
+    return static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+}
+
 // Eight consecutive elements of one K or V row: bf16 x (16 bytes) becomes
 // eight e4m3 codes e4m3(x / scale) -- one IEEE fp32 division each, rounding
 // to nearest even, saturating at +-448 -- stored as 8 bytes at dst; or, for
@@ -66,18 +78,8 @@ __device__ __forceinline__ void store_row_part(void *dst_row, int part, uint4 x,
     if constexpr (kBf16Cache) {
         *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst_row) + part * 8) = x;
     } else {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t packed[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float2 p0 = bf16x2_to_f32x2(w[2 * i]);
-            const float2 p1 = bf16x2_to_f32x2(w[2 * i + 1]);
-            const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(p0.x, scale), __fdiv_rn(p0.y, scale));
-            const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(p1.x, scale), __fdiv_rn(p1.y, scale));
-            packed[i] = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
-        }
         *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(dst_row) + part * 8) =
-            make_uint2(packed[0], packed[1]);
+            make_uint2(encode4_e4m3(x.x, x.y, scale), encode4_e4m3(x.z, x.w, scale));
     }
 }
 

@@ -206,8 +206,9 @@ KVQ_API kvq_status kvq_quantize_pages(const kvq_cache_desc *src_desc, const void
  *                  ceil(max_pages_per_seq * page_size / *split_tokens).
  *   *workspace_bytes OUT: bytes of workspace kvq_decode_attn needs: the
  *                  arrival counters (4 bytes per request and KV head, padded
- *                  to 256) plus, when a request can span more than one
- *                  split, the per-split partial results.
+ *                  to 256) plus, when a request can span more than one split
+ *                  and the splits merge through the workspace, the per-split
+ *                  partial results.
  * Any OUT pointer may be NULL.
  */
 KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, int32_t num_q_heads,
@@ -243,9 +244,12 @@ KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, in
  *                  per-split partial results (lse, o) of one call.  Two calls
  *                  in flight at once must not share a workspace.
  *   num_splits     as in kvq_decode_plan.
- * One kernel launch: every (split, KV head, request) is one CTA; the last
- * split of a (request, KV head) to finish merges the splits' partials by
- * their log-sum-exp weights (the combine) before it exits.
+ * One kernel launch: every (split, KV head, request) is one CTA.  The
+ * splits' partials are merged by their log-sum-exp weights (the combine)
+ * inside the launch: when the splits of every (request, KV head) fit on the
+ * GPU at once as one thread-block cluster each, through distributed shared
+ * memory; otherwise the last split of a (request, KV head) to finish merges
+ * them from the workspace before it exits.
  */
 KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t batch,
                            int32_t num_q_heads, const void *k_cache, const void *v_cache,
@@ -255,6 +259,36 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, in
                            const uint8_t *abort_flags, void *out, int32_t out_dtype,
                            void *workspace, size_t workspace_bytes, int32_t num_splits,
                            kvq_stream_t stream);
+
+/*
+ * kvq_decode_attn_append -- kvq_append of each request's new token followed
+ * by kvq_decode_attn, in one launch.  Request r's new token is the last one
+ * it attends to: position seq_lens[r] - 1, written at
+ *   slot = block_table[r][(seq_lens[r] - 1) / page_size] * page_size
+ *          + (seq_lens[r] - 1) % page_size,
+ * with the codes kvq_append would write (blog post "Smaller, faster, safer",
+ * page-1 mirror section "量化KV缓存": quantise on append; FP8 attention that
+ * converts what it reads).
+ *
+ *   k_new, v_new   bf16 [B][Hkv][D], 16-byte aligned: row r is request r's
+ *                  new token.
+ *   k_cache, v_cache  written (one row per request and KV head) and read.
+ *   Every other argument as in kvq_decode_attn.
+ * Results equal kvq_append(k_new, v_new, slots as above, abort_flags) then
+ * kvq_decode_attn with the same arguments, bit for bit.  A request that is
+ * aborted, empty, longer than its table row or that names a page outside
+ * [0, num_pages) gets zeros and no write.  Only request r's own last page
+ * is written, so the rows of different requests must not share a page
+ * position.
+ */
+KVQ_API kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                  int32_t num_q_heads, void *k_cache, void *v_cache,
+                                  const float *k_scale, const float *v_scale,
+                                  const int32_t *block_table, int32_t max_pages_per_seq,
+                                  const int32_t *seq_lens, float softmax_scale,
+                                  const uint8_t *abort_flags, const void *k_new, const void *v_new,
+                                  void *out, int32_t out_dtype, void *workspace,
+                                  size_t workspace_bytes, int32_t num_splits, kvq_stream_t stream);
 
 /*
  * kvq_decode_attn_static_ws -- kvq_decode_attn for callers that cannot

@@ -302,9 +302,10 @@ class ChurnGraphStep:
     CUDA graph and replayed each step after the step's tables and values are
     copied in."""
 
-    def __init__(self, dev: ChurnDevice):
+    def __init__(self, dev: ChurnDevice, fused_append: bool = False):
         torch = dev.torch
         self.dev, s = dev, dev.s
+        self.fused_append = fused_append      # append inside each layer's decode launch
         B, maxp, d = s.batch, s.max_pages, dev.device
         self.bt = torch.empty((B, maxp), dtype=torch.int32, device=d)
         self.exp = torch.empty((B, maxp), dtype=torch.int32, device=d)
@@ -340,6 +341,11 @@ class ChurnGraphStep:
         dev, kvq, s = self.dev, self.dev.kvq, self.dev.s
         kvq.kvq_tag_check(self.bt, self.exp, self.seq, s.ps, self.tags, dev.abort, stream)
         for l in range(dev.layers):
+            if self.fused_append:
+                kvq.kvq_decode_attn_append(dev.desc, self.q[l], dev.k[l], dev.v[l], dev.k_scale[l],
+                                           dev.v_scale[l], self.bt, self.seq, dev.sigma, dev.abort,
+                                           self.kn[l], self.vn[l], self.out[l], dev.ws, 0, stream)
+                continue
             kvq.kvq_append(dev.desc, self.kn[l], self.vn[l], self.slots, dev.k_scale[l], dev.v_scale[l],
                            dev.abort, dev.k[l], dev.v[l], stream)
             kvq.kvq_decode_attn(dev.desc, self.q[l], dev.k[l], dev.v[l], dev.k_scale[l], dev.v_scale[l],

@@ -320,3 +320,77 @@ def test_tag_check_append_matches_the_two_oracle_passes(bf16):
                   dw.k_scale_host, dw.v_scale_host, flags, page_size=16)
     assert np.array_equal(to_np_bits(dw.k_cache), kc_ref)
     assert np.array_equal(to_np_bits(dw.v_cache), vc_ref)
+
+
+# ------------------------------------------------- fused append + attention
+
+def _fused_vs_separate(w, cd, fp32, splits, abort=None, fill=None):
+    """Run the separate (append, then decode) and the fused call on two copies
+    of the same workload.  fill: cache bytes to start from instead of the
+    populated prefill (same for both)."""
+    sep = DeviceWorkload(w, cd, populate=fill is None)
+    fus = DeviceWorkload(w, cd, populate=fill is None)
+    if fill is not None:
+        for dw in (sep, fus):
+            dw.k_cache.copy_(torch.from_numpy(fill[0]))
+            dw.v_cache.copy_(torch.from_numpy(fill[1]))
+    ab = None if abort is None else torch.from_numpy(abort).to(DEV)
+    out_s, out_f = sep.out(fp32), fus.out(fp32)
+    sep.append(ab)
+    sep.attend(out_s, sep.workspace(splits), ab, splits)
+    kvq.kvq_decode_attn_append(fus.desc, fus.q, fus.k_cache, fus.v_cache, fus.k_scale, fus.v_scale,
+                               fus.block_table, fus.seq_lens, w.softmax_scale, ab, fus.k_new,
+                               fus.v_new, out_f, fus.workspace(splits), splits)
+    torch.cuda.synchronize()
+    return sep, fus, out_s, out_f
+
+
+@pytest.mark.parametrize("cache", ["fp8", "bf16"])
+@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("splits", [0, 1, 5, 12])
+def test_decode_attn_append_equals_append_then_decode(cache, ps, splits):
+    """kvq_decode_attn_append == kvq_append (token r at position L_r - 1) then
+    kvq_decode_attn: caches and outputs bit for bit, both forms of the
+    combine; and the output matches the oracle."""
+    cd = kvq.KVQ_CACHE_FP8_E4M3 if cache == "fp8" else kvq.KVQ_CACHE_BF16
+    w = W.make_custom(LENS, group=4, page_size=ps, seed=40 + ps + splits, outlier_frac=0.01)
+    abort = np.zeros(w.batch, np.uint8)
+    abort[3] = 1
+    for fp32 in (False, True):
+        sep, fus, out_s, out_f = _fused_vs_separate(w, cd, fp32, splits, abort)
+        assert torch.equal(fus.k_cache, sep.k_cache) and torch.equal(fus.v_cache, sep.v_cache)
+        assert torch.equal(out_f.view(torch.int32 if fp32 else torch.int16),
+                           out_s.view(torch.int32 if fp32 else torch.int16))
+    kc, vc = oracle_caches(fus, [r for r in range(w.batch) if not abort[r]])
+    # the aborted request's new token is not written: the oracle caches hold
+    # its prefill only
+    r = 3
+    L = int(w.seq_lens[r])
+    k, v, _ = fus.host_request(r)
+    oracle.append(kc, vc, k[:L - 1], v[:L - 1], w.slots_of(r, np.arange(L - 1)),
+                  fus.k_scale_host, fus.v_scale_host, page_size=w.page_size)
+    assert np.array_equal(to_np_bits(fus.k_cache), kc) and np.array_equal(to_np_bits(fus.v_cache), vc)
+    ref = oracle_attention(fus, kc, vc, abort)
+    assert_close(out_to_np(out_f), ref, "fp32", f"fused {cache} ps{ps} splits{splits}")
+
+
+def test_decode_attn_append_edge_requests():
+    """Empty, too-long and bad-page requests: zeros, and the cache is written
+    exactly where kvq_append would write it."""
+    lens = [40, 0, 77, 300, 5, 64]
+    w = W.make_custom(lens, group=4, page_size=16, seed=3)
+    w.block_table[2, 1] = w.num_pages + 1            # bad id in another page than the last
+    w.block_table[3, 18] = -7                         # bad id: the request's last page
+    w.seq_lens[4] = w.block_table.shape[1] * 16 + 3   # longer than its table row
+    rng = np.random.default_rng(8)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    fill = (rng.choice(finite, size=w.cache_shape()).astype(np.uint8),
+            rng.choice(finite, size=w.cache_shape()).astype(np.uint8))
+    for splits in (1, 0, 4, 12):
+        sep, fus, out_s, out_f = _fused_vs_separate(w, kvq.KVQ_CACHE_FP8_E4M3, True, splits,
+                                                    fill=fill)
+        assert torch.equal(fus.k_cache, sep.k_cache) and torch.equal(fus.v_cache, sep.v_cache)
+        got = out_to_np(out_f)
+        for r in (1, 2, 3, 4):
+            assert np.all(got[r] == 0.0), (splits, r)
+        assert torch.equal(out_f.view(torch.int32), out_s.view(torch.int32))
