@@ -11,44 +11,88 @@
 //                                 element by element e4m3(x / scale[h]) --
 //                                 the append rule on every slot
 // All three are plain HBM streams: the amax pass reads 2 B per element, the
-// quantise pass reads 2 B and writes 1 B per element.
+// quantise pass reads 2 B and writes 1 B per element.  Both run one wave of
+// 256-thread CTAs (8 per SM for amax, 4 for quantise); a warp streams one
+// (page, head) tile at a time with eight 16-byte loads in flight per lane.
 #include "kvq_rowops.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kHandoffThreads = 256;
+constexpr int kHandoffWarps = kHandoffThreads / 32;
+constexpr int kVecsPerLane = 8;          // 16-byte loads in flight per lane
+constexpr int kCtasPerSmAmax = 8;        // 2,048 threads per SM
+constexpr int kCtasPerSmQuant = 4;       // 1,024 threads per SM (64 registers each)
 
-// One CTA per (listed page, KV head, K|V): max |x| of the ps x 128 tile,
-// folded into amax_bits[kv][h] with an integer max on the float's bits
-// (valid because every value folded is non-negative).
-__global__ void __launch_bounds__(kHandoffThreads) amax_kernel(HandoffArgs a)
+int device_sms()
 {
-    const int i = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
-    const int32_t page = a.src_pages[i];
-    if (page < 0 || page >= a.src_num_pages)
-        return;
-    const uint16_t *src = static_cast<const uint16_t *>(kv ? a.v_src : a.k_src) +
-                          (static_cast<int64_t>(page) * a.num_kv_heads + h) * a.page_size * kHeadDim;
-    const int vecs = a.page_size * kHeadDim / 8;
-    float m = 0.f;
-    for (int v = threadIdx.x; v < vecs; v += kHandoffThreads) {
-        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 148;
+    if (dev < 64 && cache[dev] > 0)
+        return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev < 64)
+        cache[dev] = n;
+    return n;
+}
+
+__device__ __forceinline__ float absmax8(uint4 x, float m)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = bf16x2_to_f32x2(w[j]);
-            m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = bf16x2_to_f32x2(w[k]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+    return m;
+}
+
+// CTA (x = K|V x KV head, y): its warps take every (gridDim.y x 8)-th listed
+// page, one page's (ps x 128) tile of the CTA's head at a time, eight 16-byte
+// loads in flight per lane; the next page id is loaded while the current tile
+// streams.  The CTA's max |x| is folded into amax_bits[kv][h] with an integer
+// max on the float's bits (valid because every value folded is non-negative).
+__global__ void __launch_bounds__(kHandoffThreads, kCtasPerSmAmax) amax_kernel(HandoffArgs a)
+{
+    const int kv = blockIdx.x / a.num_kv_heads, h = blockIdx.x % a.num_kv_heads;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int per_tile = a.page_size * kHeadDim / 8;             // 16-byte vectors per tile
+    const int64_t step = static_cast<int64_t>(gridDim.y) * kHandoffWarps;
+    const uint4 *base = reinterpret_cast<const uint4 *>(kv ? a.v_src : a.k_src);
+    float m = 0.f;
+    int64_t i = static_cast<int64_t>(blockIdx.y) * kHandoffWarps + warp;
+    int32_t page = i < a.num_listed ? __ldg(a.src_pages + i) : -1;
+    for (; i < a.num_listed; i += step) {
+        const int32_t next = i + step < a.num_listed ? __ldg(a.src_pages + i + step) : -1;
+        if (page >= 0 && page < a.src_num_pages) {
+            const uint4 *tile = base + (static_cast<int64_t>(page) * a.num_kv_heads + h) * per_tile;
+            for (int e0 = 0; e0 < per_tile; e0 += 32 * kVecsPerLane) {
+                uint4 x[kVecsPerLane];
+#pragma unroll
+                for (int k = 0; k < kVecsPerLane; ++k) {
+                    const int e = e0 + k * 32 + lane;
+                    x[k] = e < per_tile ? __ldg(tile + e) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < kVecsPerLane; ++k)
+                    m = absmax8(x[k], m);
+            }
         }
+        page = next;
     }
     for (int off = 16; off > 0; off >>= 1)
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    __shared__ float red[kHandoffThreads / 32];
-    if (threadIdx.x % 32 == 0)
-        red[threadIdx.x / 32] = m;
+    __shared__ float red[kHandoffWarps];
+    if (lane == 0)
+        red[warp] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kHandoffThreads / 32; ++w)
+        for (int w = 1; w < kHandoffWarps; ++w)
             m = fmaxf(m, red[w]);
         atomicMax(reinterpret_cast<unsigned int *>(kv ? a.v_scale_out : a.k_scale_out) + h,
                   __float_as_uint(m));
@@ -65,32 +109,51 @@ __global__ void scales_kernel(HandoffArgs a)
     }
 }
 
-// 16 rows (of 128 elements) per CTA; rows enumerate (listed page, K|V, KV
-// head, slot).  A listed pair whose source or destination page id is out of
-// range is skipped.
-__global__ void __launch_bounds__(kHandoffThreads) quantize_pages_kernel(HandoffArgs a)
+// One warp per (listed pair, K|V, KV head) tile at a time, grid-stride over
+// the tiles; eight 16-byte loads (64 bf16 elements) in flight per lane; the
+// next tile's page ids are loaded while the current one streams.  Every
+// element becomes e4m3(x / scale[h]) by the append rule.  A listed pair whose
+// source or destination page id is out of range is skipped.
+__global__ void __launch_bounds__(kHandoffThreads, kCtasPerSmQuant) quantize_pages_kernel(HandoffArgs a)
 {
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * (kHandoffThreads / kThreadsPerRow) +
-                        threadIdx.x / kThreadsPerRow;
-    const int part = threadIdx.x % kThreadsPerRow;
-    const int64_t rows_per_page = 2LL * a.num_kv_heads * a.page_size;
-    if (row >= rows_per_page * a.num_listed)
-        return;
-    const int64_t i = row / rows_per_page;
-    const int64_t rem = row % rows_per_page;
-    const int kv = static_cast<int>(rem / (static_cast<int64_t>(a.num_kv_heads) * a.page_size));
-    const int h = static_cast<int>((rem / a.page_size) % a.num_kv_heads);
-    const int slot = static_cast<int>(rem % a.page_size);
-    const int32_t sp = __ldg(a.src_pages + i), dp = __ldg(a.dst_pages + i);
-    if (sp < 0 || sp >= a.src_num_pages || dp < 0 || dp >= a.dst_num_pages)
-        return;
-    const int64_t src_row = (static_cast<int64_t>(sp) * a.num_kv_heads + h) * a.page_size + slot;
-    const int64_t dst_row = (static_cast<int64_t>(dp) * a.num_kv_heads + h) * a.page_size + slot;
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(
-        static_cast<const uint16_t *>(kv ? a.v_src : a.k_src) + src_row * kHeadDim + part * 8));
-    const float scale = __ldg((kv ? a.v_scale : a.k_scale) + h);
-    store_row_part<false>(static_cast<uint8_t *>(kv ? a.v_dst : a.k_dst) + dst_row * kHeadDim, part, x,
-                          scale);
+    const int lane = threadIdx.x % 32;
+    const int per_tile = a.page_size * kHeadDim / 8;
+    const int64_t tiles = 2LL * a.num_kv_heads * a.num_listed;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kHandoffWarps;
+    int64_t t = static_cast<int64_t>(blockIdx.x) * kHandoffWarps + threadIdx.x / 32;
+    auto ids = [&](int64_t tile) {
+        const int64_t i = tile / (2LL * a.num_kv_heads);
+        return make_int2(__ldg(a.src_pages + i), __ldg(a.dst_pages + i));
+    };
+    int2 cur = t < tiles ? ids(t) : make_int2(-1, -1);
+    for (; t < tiles; t += step) {
+        const int2 next = t + step < tiles ? ids(t + step) : make_int2(-1, -1);
+        const int h = static_cast<int>(t % a.num_kv_heads);
+        const int kv = static_cast<int>((t / a.num_kv_heads) % 2);
+        if (cur.x >= 0 && cur.x < a.src_num_pages && cur.y >= 0 && cur.y < a.dst_num_pages) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(kv ? a.v_src : a.k_src) +
+                               (static_cast<int64_t>(cur.x) * a.num_kv_heads + h) * per_tile;
+            uint2 *dst = reinterpret_cast<uint2 *>(kv ? a.v_dst : a.k_dst) +
+                         (static_cast<int64_t>(cur.y) * a.num_kv_heads + h) * per_tile;
+            const float scale = __ldg((kv ? a.v_scale : a.k_scale) + h);
+            for (int e0 = 0; e0 < per_tile; e0 += 32 * kVecsPerLane) {
+                uint4 x[kVecsPerLane];
+#pragma unroll
+                for (int k = 0; k < kVecsPerLane; ++k) {
+                    const int e = e0 + k * 32 + lane;
+                    x[k] = e < per_tile ? __ldg(src + e) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < kVecsPerLane; ++k) {
+                    const int e = e0 + k * 32 + lane;
+                    if (e < per_tile)
+                        dst[e] = make_uint2(encode4_e4m3(x[k].x, x[k].y, scale),
+                                            encode4_e4m3(x[k].z, x[k].w, scale));
+                }
+            }
+        }
+        cur = next;
+    }
 }
 
 } // namespace
@@ -103,7 +166,13 @@ cudaError_t launch_amax_scales(const HandoffArgs &a, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     if (a.num_listed > 0) {
-        const dim3 grid(static_cast<unsigned>(a.num_listed), static_cast<unsigned>(a.num_kv_heads), 2);
+        // about kCtasPerSmAmax CTAs per SM in all (one wave), every CTA on one head
+        const int heads2 = 2 * a.num_kv_heads;
+        int64_t py = static_cast<int64_t>(device_sms()) * kCtasPerSmAmax / heads2;
+        const int64_t most = (a.num_listed + kHandoffWarps - 1) / kHandoffWarps;
+        py = py < 1 ? 1 : (py > most ? most : py);
+        py = py > 65535 ? 65535 : py;
+        const dim3 grid(static_cast<unsigned>(heads2), static_cast<unsigned>(py));
         amax_kernel<<<grid, kHandoffThreads, 0, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess)
@@ -115,13 +184,12 @@ cudaError_t launch_amax_scales(const HandoffArgs &a, cudaStream_t stream)
 
 cudaError_t launch_quantize_pages(const HandoffArgs &a, cudaStream_t stream)
 {
-    const int64_t rows = 2LL * a.num_kv_heads * a.page_size * a.num_listed;
-    if (rows == 0)
+    const int64_t tiles = 2LL * a.num_kv_heads * a.num_listed;
+    if (tiles == 0)
         return cudaSuccess;
-    const int64_t per_block = kHandoffThreads / kThreadsPerRow;
-    const int64_t blocks = (rows + per_block - 1) / per_block;
-    if (blocks > 0x7FFFFFFF)
-        return cudaErrorInvalidValue;
+    int64_t blocks = static_cast<int64_t>(device_sms()) * kCtasPerSmQuant;
+    const int64_t need = (tiles + kHandoffWarps - 1) / kHandoffWarps;
+    blocks = blocks < need ? blocks : need;
     quantize_pages_kernel<<<static_cast<unsigned>(blocks), kHandoffThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }

@@ -83,3 +83,33 @@ def test_decode_over_handed_over_pages():
     ref = oracle.decode_attn(to_np_bits(q), kref, vref, ref_ks, ref_vs, dst.reshape(1, -1),
                              np.array([L], np.int32), float(np.float32(1 / np.sqrt(128))))
     assert_close(out_to_np(out), ref, "fp32", "handoff then decode")
+
+
+def test_handoff_full_size_sampled_pages():
+    """uniform8-sized prefill (4,104 bf16 pages of 8 heads x 16 tokens): scales
+    bit-exact over all pages; sampled destination pages bit-exact."""
+    ps, H, N = 16, 8, 8 * 513
+    ksrc, vsrc = _bf16_cache(N, H, ps, 21), _bf16_cache(N, H, ps, 22, scale=7.0)
+    rng = np.random.default_rng(2)
+    src = rng.permutation(N).astype(np.int32)
+    dst = rng.permutation(N).astype(np.int32)
+    src_desc = kvq.CacheDesc(N, ps, H, 128, kvq.KVQ_CACHE_BF16)
+    dst_desc = kvq.CacheDesc(N, ps, H, 128, kvq.KVQ_CACHE_FP8_E4M3)
+    ks = torch.empty(H, dtype=torch.float32, device=DEV)
+    vs = torch.empty(H, dtype=torch.float32, device=DEV)
+    kvq.kvq_amax_scales(src_desc, ksrc, vsrc, torch.from_numpy(src).to(DEV), ks, vs)
+    kd = torch.empty((N, H, ps, 128), dtype=torch.uint8, device=DEV)
+    vd = torch.empty_like(kd)
+    kvq.kvq_quantize_pages(src_desc, ksrc, vsrc, torch.from_numpy(src).to(DEV), dst_desc, kd, vd,
+                           torch.from_numpy(dst).to(DEV), ks, vs)
+    torch.cuda.synchronize()
+    kbits, vbits = to_np_bits(ksrc), to_np_bits(vsrc)
+    ref_ks, ref_vs = oracle.amax_scales(kbits, vbits, src)
+    assert np.array_equal(ks.cpu().numpy(), ref_ks) and np.array_equal(vs.cpu().numpy(), ref_vs)
+    pick = rng.choice(N, size=24, replace=False)
+    kref = np.zeros((N, H, ps, 128), np.uint8)
+    vref = np.zeros_like(kref)
+    oracle.quantize_pages(kbits, vbits, src[pick], kref, vref, dst[pick], ref_ks, ref_vs)
+    got_k, got_v = to_np_bits(kd), to_np_bits(vd)
+    assert np.array_equal(got_k[dst[pick]], kref[dst[pick]])
+    assert np.array_equal(got_v[dst[pick]], vref[dst[pick]])
