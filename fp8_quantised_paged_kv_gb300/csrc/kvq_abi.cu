@@ -13,7 +13,7 @@ using kvq::kChunkTokens;
 using kvq::kHeadDim;
 
 constexpr int kMaxSplitTokens = 8192;
-constexpr int kMinAutoSplitTokens = 256;
+constexpr int kMinAutoSplitTokens = 128;   // one 32-token chunk per warp
 constexpr int kMaxSplitsTotal = 1024;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -63,7 +63,9 @@ struct Plan {
 // Automatic split count per (request, KV head).  Large jobs use the largest
 // split (8,192 tokens): there are many waves of CTAs anyway.  Small jobs pick
 // the count whose CTAs best fill whole waves of the resident CTA slots (SMs x
-// CTAs per SM), preferring fewer waves, with splits of at least 256 tokens.
+// CTAs per SM), preferring fewer waves, with splits of at least 128 tokens
+// (one 32-token chunk per warp: a short job finishes sooner in more, shorter
+// splits).
 int64_t auto_splits(int64_t pairs, int64_t max_ctx, int64_t slots)
 {
     const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
