@@ -14,7 +14,6 @@ using kvq::kHeadDim;
 
 constexpr int kMaxSplitTokens = 8192;
 constexpr int kMinAutoSplitTokens = 128;   // one 32-token chunk per warp
-constexpr int kMaxSplitsTotal = 1024;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -74,8 +73,8 @@ int64_t auto_splits(int64_t pairs, int64_t max_ctx, int64_t slots)
     int64_t most = max_ctx / kMinAutoSplitTokens;
     if (most < 1)
         most = 1;
-    if (most > kMaxSplitsTotal)
-        most = kMaxSplitsTotal;
+    if (most > kvq::kMaxSplitsTotal)
+        most = kvq::kMaxSplitsTotal;
     int64_t best = 1;
     double best_score = -1.0;
     for (int64_t n = 1; n <= most; ++n) {
@@ -137,7 +136,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (split > kMaxSplitTokens)
         split = kMaxSplitTokens;
     int64_t splits = (max_ctx + split - 1) / split;
-    if (splits > kMaxSplitsTotal)
+    if (splits > kvq::kMaxSplitsTotal)
         return KVQ_ERR_UNSUPPORTED;
     p->split_tokens = static_cast<int32_t>(split);
     p->max_splits = static_cast<int32_t>(splits);

@@ -109,8 +109,10 @@ __device__ __forceinline__ int merge_col(int d) { return d + 2 * (d >> 5); }
 // warps' merge area, inside the ring (idle by then).
 constexpr int kScratchOffset =
     (kWarps * kMaxGroup * kMergeStride + 3 * kWarps * kMaxGroup + 2 * kMaxGroup + 3) / 4 * 4;
+static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kMaxSplitsTotal) * 4 <= Tile<false>::kRingBytes,
+              "the workspace combine's scratch fits in the idle ring");
 static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kHeadDim) * 4 <= Tile<false>::kRingBytes,
-              "combine scratch and cluster partial fit in the idle ring");
+              "the cluster combine's partial fits in the idle ring");
 
 // Count this split's arrival for (request b, KV head kvh).  The last split
 // to arrive merges the partials of all nsplit splits of the group:

@@ -13,6 +13,7 @@ constexpr int kHeadDim = 128;
 constexpr int kChunkTokens = 32;     // tokens one warp consumes per pipeline stage
 constexpr int kMaxGroup = 8;         // query heads per KV head on one mma n-tile
 constexpr int kMaxCluster = 8;       // splits merged inside one thread-block cluster
+constexpr int kMaxSplitsTotal = 1024;  // splits of one (request, KV head)
 
 struct AppendArgs {
     const void *k_new, *v_new;       // bf16 [T][Hkv][D]
