@@ -78,6 +78,8 @@ def _load():
     lib.oracle_amax_scales.restype = None
     lib.oracle_quantize_pages.argtypes = [i32, i32, i32, P, P, P, P, P, P, i32, P, P]
     lib.oracle_quantize_pages.restype = None
+    lib.oracle_w4a16_gemm.argtypes = [i32, i32, i32, P, P, P, P]
+    lib.oracle_w4a16_gemm.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     _lib = lib
@@ -211,3 +213,20 @@ def quantize_pages(k_src, v_src, src_pages, k_dst, v_dst, dst_pages, k_scale, v_
     lib.oracle_quantize_pages(Hkv, D, ps, _ptr(ks_), _ptr(vs_), _ptr(sp), _ptr(k_dst), _ptr(v_dst),
                               _ptr(dp), sp.size, _ptr(_c(k_scale, np.float32)),
                               _ptr(_c(v_scale, np.float32)))
+
+
+def w4a16_gemm(x_bits, w_packed, scale_bits):
+    """y[m][n] = sum_k x[m][k] * q[n][k] * s[n][k / 128] in fp64.
+
+    x_bits: uint16 bf16 bits [M][K]; w_packed: uint8 [N][K / 2] (low nibble =
+    even k, two's complement); scale_bits: uint16 bf16 bits [N][K / 128]."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    w = _c(w_packed, np.uint8)
+    sc = _c(scale_bits, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    assert K % 128 == 0 and w.shape == (N, K // 2) and sc.shape == (N, K // 128)
+    y = np.empty((M, N), np.float64)
+    lib.oracle_w4a16_gemm(M, N, K, _ptr(x), _ptr(w), _ptr(sc), _ptr(y))
+    return y

@@ -369,3 +369,42 @@ void oracle_quantize_pages(int32_t num_kv_heads, int32_t head_dim, int32_t page_
         }
     }
 }
+
+/*
+ * INT4 weight-only product for decode (the pages' second technique: weights
+ * compressed from FP8 to 4-bit integers, expanded before the multiply;
+ * page 1, section "Compressing model weights"; page 2, "Model weight
+ * compression to lower latency").  The pages fix no format; the reading
+ * taken here:
+ *   - w[n][k] = q[n][k] * s[n][k / 128]: symmetric signed 4-bit integers
+ *     q in [-8, 7] (two's complement), one bf16 scale per output column n
+ *     and group of 128 consecutive k;
+ *   - packing: byte k / 2 of row n of W (rows of K / 2 bytes) holds q[n][k]
+ *     in its low nibble for even k, in its high nibble for odd k;
+ *   - y[m][n] = sum_k x[m][k] * w[n][k], x bf16.
+ * fp64 throughout; one output column per outer iteration.
+ */
+static int oracle_int4_nibble(uint8_t byte, int64_t k)
+{
+    int v = (k & 1) ? (byte >> 4) : (byte & 0x0F);
+    return v >= 8 ? v - 16 : v;
+}
+
+void oracle_w4a16_gemm(int32_t m, int32_t n, int32_t k, const uint16_t *x, const uint8_t *w,
+                       const uint16_t *scales, double *y)
+{
+    const int32_t groups = k / 128;
+#pragma omp parallel for schedule(static)
+    for (int32_t col = 0; col < n; ++col) {
+        const uint8_t *wrow = w + (int64_t)col * (k / 2);
+        for (int32_t row = 0; row < m; ++row) {
+            double acc = 0.0;
+            for (int64_t kk = 0; kk < k; ++kk) {
+                double s = (double)bf16_bits_to_float(scales[(int64_t)col * groups + kk / 128]);
+                double wv = (double)oracle_int4_nibble(wrow[kk / 2], kk) * s;
+                acc += (double)bf16_bits_to_float(x[(int64_t)row * k + kk]) * wv;
+            }
+            y[(int64_t)row * n + col] = acc;
+        }
+    }
+}
