@@ -631,6 +631,67 @@ def run_handoff(args):
     return 0
 
 
+def run_w4a16(args):
+    """INT4 weight-only product for decode: y = x W^T, W int4 [N][K/2] with a
+    bf16 scale per column and 128-k group, x bf16 [M][K].  Shape: K = 8,192,
+    N = 24,576 (100.7 MB of packed weights and scales, larger than L2); batch
+    rows M = 1 (the value), 4 and 16.  Reports the weight bytes streamed per
+    second against the measured HBM peak."""
+    import torch
+    import fp8_quantised_paged_kv_gb300 as kvq
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    kvq.load()
+    kvq.kvq_device_error(clear=True)
+    K, N = 8192, 24576
+    g = torch.Generator(device=dev)
+    g.manual_seed(rank)
+    w = torch.randint(0, 256, (N, K // 2), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    sc = (torch.rand((N, K // 128), generator=g, device=dev) * 0.04 - 0.02).to(torch.bfloat16)
+    wbytes = w.numel() + sc.numel() * 2
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    per_m = {}
+    for M in (1, 4, 16):
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            kvq.kvq_w4a16_gemm(x, w, sc, y)
+            e1.record(stream)
+            if i >= args.warmup:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+        per_m[M] = {"us": round(ms * 1e3, 2), "weight_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+                    "splits": kvq.kvq_w4a16_plan(M, N, K)}
+    main = per_m[1]
+    if rank == 0:
+        print(json.dumps({
+            "metric": "INT4 weight-only decode product: weight bytes streamed per second",
+            "value": main["weight_gbs"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(main["us"] / 1e3, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xbf16",
+            "data": "synthetic",
+            "config": {"workload": "w4a16", "m": 1, "k": K, "n": N, "group": 128,
+                       "weight_bytes": wbytes, "l2": "flushed before every timed step (512 MiB write)"},
+            "roofline": {"bound": "hbm", "kernel": "w4a16_kernel", "achieved": main["weight_gbs"],
+                         "peak": peak, "unit": "GB/s", "frac": round(main["weight_gbs"] / peak, 4),
+                         "traffic": None, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": wbytes},
+            "by_batch_rows": per_m,
+            "gpu_launches": args.steps * 3,
+            "device_error_bits": kvq.kvq_device_error(),
+        }))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -659,6 +720,8 @@ def main():
         return run_churn(args)
     if args.workload == "handoff":
         return run_handoff(args)
+    if args.workload == "w4a16":
+        return run_w4a16(args)
     return run_ours(args)
 
 

@@ -10,6 +10,9 @@ missing the calls raise.
     kvq_append(...)         quantise-on-append of new K/V into paged slots
     kvq_decode_attn(...)    split-K paged decode attention + LSE combine
     kvq_decode_plan(...)    split / workspace sizes for kvq_decode_attn
+    kvq_decode_attn_append(...), kvq_tag_check_append(...)   fused forms
+    kvq_amax_scales(...), kvq_quantize_pages(...)            prefill -> decode handoff
+    kvq_w4a16_gemm(...)     INT4 weight-only product for decode
 """
 from __future__ import annotations
 
@@ -63,6 +66,8 @@ _SIGS = {
                         "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_decode_attn_append": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
                                "p", "p", "p", "p", "i32", "p", "size", "i32", "p"],
+    "kvq_w4a16_plan": ["i32", "i32", "i32", "i32", "p"],
+    "kvq_w4a16_gemm": ["p", "p", "p", "i32", "i32", "i32", "p", "i32", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
     "kvq_amax_scales": ["desc", "p", "p", "p", "i32", "p", "p", "p"],
     "kvq_quantize_pages": ["desc", "p", "p", "p", "desc", "p", "p", "p", "i32", "p", "p", "p"],
@@ -279,6 +284,31 @@ def kvq_decode_attn_append(desc, q, k_cache, v_cache, k_scale, v_scale, block_ta
         out_dtype, _ptr(workspace), ws_bytes, num_splits, _stream(stream))
     _check("kvq_decode_attn_append", st)
     return out
+
+
+def kvq_w4a16_plan(m: int, n: int, k: int, num_splits: int = 0) -> int:
+    """Split count of K that kvq_w4a16_gemm uses for these shapes."""
+    s = ctypes.c_int32()
+    _check("kvq_w4a16_plan", load().kvq_w4a16_plan(m, n, k, num_splits, ctypes.byref(s)))
+    return s.value
+
+
+def kvq_w4a16_gemm(x, w, scales, y, num_splits: int = 0, stream=None):
+    """y = x W^T with INT4 weights: x bf16 [M][K], w uint8 [N][K/2] (signed
+    nibbles, low nibble = even k), scales bf16 [N][K/128]; y bf16 or fp32 [M][N]."""
+    import torch
+    M, K = x.shape
+    N = w.shape[0]
+    _expect(x, torch.bfloat16, (M, K), "x")
+    _expect(w, torch.uint8, (N, K // 2), "w")
+    _expect(scales, torch.bfloat16, (N, K // 128), "scales")
+    if y.dtype not in (torch.bfloat16, torch.float32) or tuple(y.shape) != (M, N):
+        raise ValueError("y: expected bf16 or fp32 [M][N]")
+    st = load().kvq_w4a16_gemm(_ptr(x), _ptr(w), _ptr(scales), M, N, K, _ptr(y),
+                               KVQ_OUT_FP32 if y.dtype == torch.float32 else KVQ_OUT_BF16,
+                               num_splits, _stream(stream))
+    _check("kvq_w4a16_gemm", st)
+    return y
 
 
 def kvq_device_error(clear: bool = False) -> int:

@@ -532,7 +532,109 @@ kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void *q, int
 
 kvq_status kvq_device_error(uint32_t *bits, int32_t clear)
 {
-    return to_status(kvq::read_device_error(bits, clear != 0));
+    uint32_t a = 0, b = 0;
+    cudaError_t e = kvq::read_device_error(&a, clear != 0);
+    if (e == cudaSuccess)
+        e = kvq::read_w4_error(&b, clear != 0);
+    if (bits)
+        *bits = a | b;
+    return to_status(e);
+}
+
+kvq_status kvq_w4a16_plan(int32_t m, int32_t n, int32_t k, int32_t num_splits, int32_t *splits)
+{
+    if (m < 0 || n < 0 || k <= 0 || num_splits < 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (k % kvq::kW4BlockK != 0 || n % kvq::kW4Cols != 0)
+        return KVQ_ERR_UNSUPPORTED;
+    // K is cut into at most kW4MaxSplits ranges of at most 8,192 k (the scales
+    // of one range are staged in shared memory) that are whole 256-k blocks.
+    auto usable = [&](int s) { return s >= 1 && s <= kvq::kW4MaxSplits && k % (s * kvq::kW4BlockK) == 0 &&
+                                      k / s <= 8192; };
+    int dev = 0;
+    const bool have_device = cudaGetDevice(&dev) == cudaSuccess;
+    if (!have_device)
+        cudaGetLastError();
+    auto runnable = [&](int s) { return s == 1 || !have_device || kvq::w4a16_cluster_capacity(s) >= 1; };
+    int best = 0;
+    if (num_splits > 0) {
+        if (!usable(num_splits) || !runnable(num_splits))
+            return KVQ_ERR_UNSUPPORTED;
+        best = num_splits;
+    } else {
+        // the count whose CTAs best fill whole waves of the resident CTA
+        // slots, preferring fewer waves and at least four 256-k blocks per
+        // warp (a warp's copies then overlap its arithmetic)
+        const int64_t tiles = n / kvq::kW4Cols;
+        const int64_t slots = static_cast<int64_t>(sm_count()) * kvq::w4a16_ctas_per_sm();
+        double best_score = -1e9;
+        for (int s = 1; s <= kvq::kW4MaxSplits; ++s) {
+            if (!usable(s) || !runnable(s))
+                continue;
+            const int64_t ctas = tiles * s;
+            const int64_t waves = (ctas + slots - 1) / slots;
+            const double fill = waves == 0 ? 0.0
+                                           : static_cast<double>(ctas) / static_cast<double>(waves * slots);
+            const int64_t blocks_per_warp = k / s / kvq::kW4BlockK / 4;
+            const double score = fill - 0.1 * static_cast<double>(waves) - (blocks_per_warp < 4 ? 0.5 : 0.0);
+            if (score > best_score + 1e-9) {
+                best_score = score;
+                best = s;
+            }
+        }
+    }
+    if (best == 0)
+        return KVQ_ERR_UNSUPPORTED;
+    if (splits)
+        *splits = best;
+    return KVQ_OK;
+}
+
+kvq_status kvq_w4a16_gemm(const void *x, const uint8_t *w, const void *scales, int32_t m, int32_t n,
+                          int32_t k, void *y, int32_t out_dtype, int32_t num_splits, kvq_stream_t stream)
+{
+    int32_t splits = 0;
+    kvq_status st = kvq_w4a16_plan(m, n, k, num_splits, &splits);
+    if (st != KVQ_OK)
+        return st;
+    if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_FP32)
+        return KVQ_ERR_INVALID_ARG;
+    if (m == 0 || n == 0)
+        return KVQ_OK;
+    if (!x || !w || !scales || !y || !aligned16(x) || !aligned16(w) || !aligned16(y))
+        return KVQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(scales) & 1u) != 0)
+        return KVQ_ERR_INVALID_ARG;
+    EncodeFn fn = encode_fn();
+    if (fn == nullptr)
+        return KVQ_ERR_CUDA;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(n)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kvq::kW4Cols)};
+    const cuuint32_t estr[2] = {1, 1};
+    std::memset(&map, 0, sizeof map);
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KVQ_ERR_CUDA;
+    const size_t out_elem = out_dtype == KVQ_OUT_FP32 ? 4 : 2;
+    for (int32_t r0 = 0; r0 < m; r0 += 16) {             // 16 rows of x per launch
+        kvq::W4Args a = {};
+        a.x = static_cast<const uint8_t *>(x) + static_cast<size_t>(r0) * k * 2;
+        a.scales = scales;
+        a.y = static_cast<uint8_t *>(y) + static_cast<size_t>(r0) * n * out_elem;
+        a.rows = m - r0 < 16 ? m - r0 : 16;
+        a.n = n;
+        a.k = k;
+        a.splits = splits;
+        a.k_split = k / splits;
+        a.out_fp32 = out_dtype == KVQ_OUT_FP32;
+        const cudaError_t e = kvq::launch_w4a16(a, map, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess)
+            return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
 }
 
 } // extern "C"

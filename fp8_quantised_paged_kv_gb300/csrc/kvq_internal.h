@@ -54,6 +54,26 @@ cudaError_t launch_quantize_pages(const HandoffArgs &a, cudaStream_t stream);
 // unless it was aborted (decode step: one new token per request).
 cudaError_t launch_tag_check_append(const TagCheckArgs &t, const AppendArgs &a, cudaStream_t stream);
 
+// INT4 weight-only product y[m][n] = sum_k x[m][k] q[n][k] s[n][k / 128] for
+// up to 16 rows of x per launch.  The weights are read through a 2-D tensor
+// map over W viewed as [N rows][K / 2 bytes].
+struct W4Args {
+    const void *x;                   // bf16 [rows][k] (this launch's rows)
+    const void *scales;              // bf16 [n][k / 128]
+    void *y;                         // [rows][n], bf16 or fp32
+    int32_t rows, n, k;              // rows <= 16; k % 256 == 0; n % 64 == 0
+    int32_t splits, k_split;         // K is cut into `splits` ranges of k_split
+    bool out_fp32;
+};
+constexpr int kW4Cols = 64;          // output columns per CTA
+constexpr int kW4BlockK = 256;       // k per copied box: 128 bytes of every column
+constexpr int kW4MaxSplits = 8;      // splits of K (one thread-block cluster)
+cudaError_t launch_w4a16(const W4Args &a, const CUtensorMap &w_map, cudaStream_t stream);
+// Resident CTAs of the INT4 kernel per SM, and resident clusters of `splits`.
+int w4a16_ctas_per_sm();
+int w4a16_cluster_capacity(int splits);
+cudaError_t read_w4_error(uint32_t *bits, bool clear);
+
 // Workspace layout (bytes from the workspace base):
 //   [0, counter_bytes)       uint32 arrivals[B][Hkv]: splits of each (request, KV
 //                            head) that have published; zero before the first

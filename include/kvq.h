@@ -291,6 +291,37 @@ KVQ_API kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void
                                   size_t workspace_bytes, int32_t num_splits, kvq_stream_t stream);
 
 /*
+ * kvq_w4a16_plan / kvq_w4a16_gemm -- INT4 weight-only product for decode
+ * (blog post "Smaller, faster, safer", page-1 mirror section "压缩模型权重":
+ * weights compressed from FP8 to 4-bit integers for decode, which streams
+ * the weights; page-2 mirror section "模型权重压缩以降低延迟"):
+ *   y[m][n] = sum_k x[m][k] * q[n][k] * s[n][k / 128]
+ * The pages fix no format; this library's:
+ *   w              uint8 [N][K/2]: byte k/2 of row n holds q[n][k], a signed
+ *                  (two's complement) 4-bit integer in [-8, 7], in its low
+ *                  nibble for even k and its high nibble for odd k.
+ *   scales         bf16 [N][K/128] (2-byte aligned): one per output column
+ *                  and group of 128 consecutive k.
+ *   x              bf16 [M][K], 16-byte aligned.  On the tensor cores x and
+ *                  the expanded weights are f16: exact for |x| in
+ *                  [2^-14, 65504] (as for q in kvq_decode_attn); q is an exact
+ *                  f16 integer and the scales apply in fp32.
+ *   y              [M][N], bf16 or fp32 per out_dtype, 16-byte aligned.
+ *   Shapes: K a positive multiple of 256 and at most 65,536; N a multiple of
+ *   64 (KVQ_ERR_UNSUPPORTED otherwise); any M >= 0 (16 rows per launch: a
+ *   batch of more than 16 rows reads the weights once per 16 rows).
+ *   num_splits     ranges K is cut into (1..8, each a whole number of 256-k
+ *                  blocks, at most 8,192 k); 0 = automatic.
+ * kvq_w4a16_plan (HOST only) returns the split count kvq_w4a16_gemm uses.
+ * A copy wait that gives up sets bit 0 of kvq_device_error and gives zeros
+ * for that launch's tile of 64 columns.
+ */
+KVQ_API kvq_status kvq_w4a16_plan(int32_t m, int32_t n, int32_t k, int32_t num_splits, int32_t *splits);
+KVQ_API kvq_status kvq_w4a16_gemm(const void *x, const uint8_t *w, const void *scales, int32_t m,
+                                  int32_t n, int32_t k, void *y, int32_t out_dtype, int32_t num_splits,
+                                  kvq_stream_t stream);
+
+/*
  * kvq_decode_attn_static_ws -- kvq_decode_attn for callers that cannot
  * allocate device memory while they decode (an engine that has already
  * handed all of its device memory to its own pool, or C code that holds no

@@ -120,3 +120,18 @@ def test_batch_limit():
     with pytest.raises(kvq.KvqError) as e:
         _plan(B=65536)
     assert e.value.status == 2
+
+
+def test_w4a16_plan_and_argument_checks():
+    import ctypes
+    lib = kvq.load()
+    assert kvq.kvq_w4a16_plan(1, 12288, 5120) in range(1, 9)
+    assert kvq.kvq_w4a16_plan(16, 64, 256, 1) == 1
+    for m, n, k, ns in [(1, 64, 200, 0), (1, 60, 256, 0), (1, 64, 256, 2), (1, 64, 65536 + 256, 0)]:
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kvq_w4a16_plan(m, n, k, ns)
+        assert e.value.status == 2                       # unsupported shape / split count
+    st = lib.kvq_w4a16_gemm(None, None, None, 1, 64, 256, None, 0, 0, None)
+    assert st == 1                                        # null pointers: invalid argument
+    st = lib.kvq_w4a16_gemm(None, None, None, 0, 64, 256, None, 0, 0, None)
+    assert st == 0                                        # empty batch: nothing to do
