@@ -33,16 +33,31 @@ sys.path.insert(0, ROOT)
 METRIC = "FP8 paged decode attn: KV-read GB/s (% of HBM peak) and decode tokens/s"
 L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_uniform8.json")
+W4_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w4a16_m1.json")
+W4_SOURCES = ("kvq_w4a16.cu", "kvq_ptx.cuh")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources of the decode kernel (the one the roofline reports)."""
+def kernel_source_hash(names=("kvq_decode.cu", "kvq_ptx.cuh")) -> str:
+    """Hash of the sources of a kernel (by default the decode kernel, the one
+    the decode roofline reports)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quantised_paged_kv_gb300", "csrc")
-    for name in ("kvq_decode.cu", "kvq_ptx.cuh"):
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def profiled_traffic(path, workload, names=("kvq_decode.cu", "kvq_ptx.cuh")):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    summary is missing, is for another workload or predates the kernel's
+    current source."""
+    if not os.path.exists(path):
+        return None
+    prof = json.load(open(path))
+    if prof.get("source_hash") == kernel_source_hash(names) and prof.get("workload") == workload:
+        return prof.get("dram_bytes_per_launch")
+    return None
 
 
 def measured_peaks():
@@ -355,11 +370,7 @@ def run_ours(args):
     dev_err = kvq.kvq_device_error()
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (attn_ms / 1e3) / 1e9
-    traffic = None
-    if os.path.exists(PROFILE_SUMMARY):
-        prof = json.load(open(PROFILE_SUMMARY))
-        if prof.get("source_hash") == kernel_source_hash() and prof.get("workload") == args.workload:
-            traffic = prof.get("dram_bytes_per_launch")
+    traffic = profiled_traffic(PROFILE_SUMMARY, args.workload)
 
     # Steady state of a small workload: R steps back to back in one CUDA
     # graph, step r on its own copy of the cache (R copies together larger
@@ -684,7 +695,8 @@ def run_w4a16(args):
                        "weight_bytes": wbytes, "l2": "flushed before every timed step (512 MiB write)"},
             "roofline": {"bound": "hbm", "kernel": "w4a16_kernel", "achieved": main["weight_gbs"],
                          "peak": peak, "unit": "GB/s", "frac": round(main["weight_gbs"] / peak, 4),
-                         "traffic": None, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": wbytes},
+                         "traffic": profiled_traffic(W4_PROFILE_SUMMARY, "w4a16", W4_SOURCES),
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": wbytes},
             "by_batch_rows": per_m,
             "gpu_launches": args.steps * 3,
             "device_error_bits": kvq.kvq_device_error(),

@@ -74,6 +74,23 @@ def test_large_shape_sampled_columns():
     assert kvq.kvq_device_error() == 0
 
 
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_bench_shape_sampled_columns(M):
+    """The shape and launch bench.py times (K 8,192, N 24,576, automatic
+    splits, bf16 out), checked on sampled columns."""
+    N, K = 24576, 8192
+    x, w, s = _case(M, N, K, 100 + M)
+    xd, wd, sd = _dev(x, w, s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    kvq.kvq_w4a16_gemm(xd, wd, sd, y)
+    torch.cuda.synchronize()
+    cols = np.random.default_rng(M).choice(N, size=64, replace=False)
+    cols = np.concatenate([cols, [0, 63, N - 64, N - 1]])
+    ref = oracle.w4a16_gemm(x, w[cols], s[cols])
+    assert_close(y.float().cpu().numpy().astype(np.float64)[:, cols], ref, "bf16", f"w4a16 bench shape M{M}")
+    assert kvq.kvq_device_error() == 0
+
+
 def test_empty_batch_writes_nothing():
     N, K = 64, 256
     _, w, s = _case(1, N, K, 5)
