@@ -91,6 +91,20 @@ def test_bench_shape_sampled_columns(M):
     assert kvq.kvq_device_error() == 0
 
 
+def test_longest_k_eight_split_cluster():
+    """K = 65,536, the longest K: eight splits of 8,192 k, one cluster of 8."""
+    M, N, K = 2, 128, 65536
+    assert kvq.kvq_w4a16_plan(M, N, K) == 8
+    x, w, s = _case(M, N, K, 21)
+    ref = oracle.w4a16_gemm(x, w, s)
+    xd, wd, sd = _dev(x, w, s)
+    y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    kvq.kvq_w4a16_gemm(xd, wd, sd, y)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy().astype(np.float64), ref, "fp32", "w4a16 K 65536")
+    assert kvq.kvq_device_error() == 0
+
+
 def test_empty_batch_writes_nothing():
     N, K = 64, 256
     _, w, s = _case(1, N, K, 5)
