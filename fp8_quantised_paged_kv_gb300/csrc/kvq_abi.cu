@@ -611,11 +611,11 @@ kvq_status kvq_w4a16_gemm(const void *x, const uint8_t *w, const void *scales, i
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(n)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
-    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kvq::kW4Cols)};
+    const cuuint32_t box[2] = {kvq::kW4CopyK / 2, static_cast<cuuint32_t>(kvq::kW4Cols)};
     const cuuint32_t estr[2] = {1, 1};
     std::memset(&map, 0, sizeof map);
     if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return KVQ_ERR_CUDA;
     const size_t out_elem = out_dtype == KVQ_OUT_FP32 ? 4 : 2;

@@ -66,7 +66,8 @@ struct W4Args {
     bool out_fp32;
 };
 constexpr int kW4Cols = 64;          // output columns per CTA
-constexpr int kW4BlockK = 256;       // k per copied box: 128 bytes of every column
+constexpr int kW4BlockK = 256;       // granularity of K and of its split ranges
+constexpr int kW4CopyK = 128;        // k per tensor copy: 64 bytes of every column, one scale group
 constexpr int kW4MaxSplits = 8;      // splits of K (one thread-block cluster)
 cudaError_t launch_w4a16(const W4Args &a, const CUtensorMap &w_map, cudaStream_t stream);
 // Resident CTAs of the INT4 kernel per SM, and resident clusters of `splits`.

@@ -10,9 +10,10 @@
 //   y[m][n] = sum_k x[m][k] * q[n][k] * s[n][k / 128]
 //
 // A CTA owns 64 output columns and one of `splits` ranges of K.  Its four
-// warps take turns over that range in 256-k blocks; a block is one 2-D
-// tensor copy (TMA, 128-byte swizzle) of 64 weight rows x 128 bytes into the
-// warp's 2-stage ring.  Per 128-k group a lane expands the nibbles of two
+// warps take turns over that range one 128-k group at a time; a group is one
+// 2-D tensor copy (TMA, 64-byte swizzle) of 64 weight rows x 64 bytes into
+// the warp's 4-stage ring, so three copies stay in flight while the warp
+// works on the fourth.  Per group a lane expands the nibbles of two
 // weight columns of each 16-column tile into exact f16 integers (nibble |
 // 0x6400 is the f16 value 1024 + nibble) and multiplies them with x on the
 // tensor cores (mma.sync m16n8k16, f16 in, fp32 accumulate).  The weight
@@ -43,8 +44,8 @@ namespace {
 constexpr int kW4Warps = 4;
 constexpr int kW4Threads = kW4Warps * 32;
 constexpr int kW4CtasPerSm = 3;
-constexpr int kW4Stages = 2;
-constexpr int kW4StageBytes = kW4Cols * 128;                   // 64 rows x 128 bytes
+constexpr int kW4Stages = 4;
+constexpr int kW4StageBytes = kW4Cols * kW4CopyK / 2;          // 64 rows x 64 bytes: one group
 constexpr int kW4WarpRing = kW4Stages * kW4StageBytes;
 constexpr int kW4RingBytes = kW4Warps * kW4WarpRing;
 constexpr int kW4MaxGroups = 64;                               // groups of one split: k_split <= 8192
@@ -55,9 +56,11 @@ constexpr uint64_t kW4WaitLimitNs = 1000000000ull;
 static_assert(16 * kW4Cols * 4 <= kW4WarpRing, "a warp's partial fits in its idle ring");
 static_assert(16 * kW4Cols * 4 <= kW4Cols * kW4ScStride * 2, "the CTA's partial fits over the scales");
 
-__device__ __forceinline__ uint32_t swz128(int line, int c)
+// Byte offset of 16-byte chunk c of row `line` in a tile of 64-byte rows
+// written by a tensor copy with 64-byte swizzle.
+__device__ __forceinline__ uint32_t swz64(int line, int c)
 {
-    return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
+    return static_cast<uint32_t>(line * 64 + ((c ^ ((line >> 1) & 3)) << 4));
 }
 
 // (a & b) ^ c
@@ -118,8 +121,8 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
     const int col0 = blockIdx.x * kW4Cols;
     const int k0 = blockIdx.y * a.k_split;
     const int kcount = a.k - k0 < a.k_split ? a.k - k0 : a.k_split;   // a multiple of 256
-    const int nblocks = kcount / kW4BlockK;
-    const int groups = kcount / 128;
+    const int nblocks = kcount / kW4CopyK;                            // copies, one group each
+    const int groups = nblocks;
     const int gtot = a.k / 128;
 
     const uint64_t policy = l2_policy_evict_first();
@@ -129,7 +132,7 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
         const int st = it % kW4Stages;
         uint64_t *bar = full + w * kW4Stages + st;
         mbar_arrive_expect_tx(bar, kW4StageBytes);
-        tma_load_2d(smem + w * kW4WarpRing + st * kW4StageBytes, &w_map, (k0 + blk * kW4BlockK) / 2, col0, bar,
+        tma_load_2d(smem + w * kW4WarpRing + st * kW4StageBytes, &w_map, (k0 + blk * kW4CopyK) / 2, col0, bar,
                     policy);
     };
     // The first copies of every warp start before the scales are read, so
@@ -189,7 +192,7 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
         }
     };
     if (my_blocks > 0)
-        load_x(k0 + warp * kW4BlockK);
+        load_x(k0 + warp * kW4CopyK);
 
     // The weights of a word (eight nibbles, k = e0 .. e7) as two f16 pairs:
     // flipping a nibble's top bit turns two's complement q into q + 8; with
@@ -212,11 +215,10 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
             break;
         }
         const uint8_t *tile = ring + st * kW4StageBytes;
-        const int blk = warp + it * kW4Warps;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {                   // the block's two 128-k groups
-            const int kg = k0 + blk * kW4BlockK + h * 128;
-            const int gl = blk * 2 + h;                 // group index within the split
+        const int blk = warp + it * kW4Warps;           // the group this copy holds
+        {
+            const int kg = k0 + blk * kW4CopyK;
+            const int gl = blk;                         // group index within the split
             // x fragments (mma B, k x batch): k-step 2j pairs (e0, e4) and
             // (e1, e5) of word j, k-step 2j+1 (e2, e6) and (e3, e7)
             uint32_t bx[kNT][8][2];
@@ -230,21 +232,16 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
                     bx[nt][2 * j + 1][0] = f16x2(bf16lo(x.y), bf16lo(x.w));
                     bx[nt][2 * j + 1][1] = f16x2(bf16hi(x.y), bf16hi(x.w));
                 }
-            // the next group's x: the block's second group, or the first of
-            // this warp's next block
-            if (h == 0)
-                load_x(kg + 128);
-            else if (it + 1 < my_blocks)
-                load_x(k0 + (blk + kW4Warps) * kW4BlockK);
+            // the x of this warp's next group
+            if (it + 1 < my_blocks)
+                load_x(kg + kW4Warps * kW4CopyK);
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {            // 16-column tiles (mma A, columns x k)
                 // words j of weight rows mt * 16 + gq and + 8: bytes 4 tq ..
-                // 4 tq + 3 of 16-byte chunk 4 h + j (k = kg + 32 j + 8 tq ..
-                // + 7); ldmatrix reads each chunk's eight rows conflict-free
-                const uint4 w0 =
-                    ldmatrix_x4(smem_addr(tile + swz128(mt * 16 + (lane & 7), 4 * h + (lane >> 3))));
-                const uint4 w1 =
-                    ldmatrix_x4(smem_addr(tile + swz128(mt * 16 + 8 + (lane & 7), 4 * h + (lane >> 3))));
+                // 4 tq + 3 of 16-byte chunk j (k = kg + 32 j + 8 tq .. + 7);
+                // ldmatrix reads each chunk's eight rows conflict-free
+                const uint4 w0 = ldmatrix_x4(smem_addr(tile + swz64(mt * 16 + (lane & 7), lane >> 3)));
+                const uint4 w1 = ldmatrix_x4(smem_addr(tile + swz64(mt * 16 + 8 + (lane & 7), lane >> 3)));
                 const uint32_t u0[4] = {w0.x, w0.y, w0.z, w0.w};
                 const uint32_t u1[4] = {w1.x, w1.y, w1.z, w1.w};
                 float part[kNT][4];
