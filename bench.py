@@ -280,6 +280,13 @@ def run_ours(args):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
+        if args.one_launch:                    # tag check + append + attention, one launch
+            if ev is not None:
+                ev[1].record(stream)
+            dw.decode_step(out, ws, args.num_splits, stream)
+            if ev is not None:
+                ev[2].record(stream)
+            return
         if args.fused_append:
             dw.tag_check(stream)               # batched tag check
         else:
@@ -382,6 +389,12 @@ def run_ours(args):
         vc = [dw.v_cache.clone() for _ in range(R)]
         def steady_steps(st):
             for r in range(R):
+                if args.one_launch:
+                    kvq.kvq_decode_step(dw.desc, dw.q, kc[r], vc[r], dw.k_scale, dw.v_scale,
+                                        dw.block_table, dw.seq_lens, dw.expected_tags, dw.page_tags,
+                                        dw.abort, w.softmax_scale, dw.k_new, dw.v_new, out, ws,
+                                        args.num_splits, st)
+                    continue
                 kvq.kvq_tag_check_append(dw.desc, dw.block_table, dw.expected_tags, dw.seq_lens,
                                          dw.page_tags, dw.k_new, dw.v_new, dw.append_slots,
                                          dw.k_scale, dw.v_scale, kc[r], vc[r], dw.abort, st)
@@ -411,8 +424,9 @@ def run_ours(args):
         steady = {"copies_of_the_cache": R, "cache_bytes_total": R * 2 * dw.k_cache.numel(),
                   "us_per_step": round(per_step_ms * 1e3, 3),
                   "kv_gbs": round(kv_bytes / (per_step_ms / 1e3) / 1e9, 2),
-                  "how": "one CUDA graph of R back-to-back steps (tag check + append, then decode), "
-                         "step r on cache copy r; L2 flushed before each replay"}
+                  "how": ("one CUDA graph of R back-to-back steps (" +
+                          ("kvq_decode_step" if args.one_launch else "tag check + append, then decode") +
+                          "), step r on cache copy r; L2 flushed before each replay")}
         del kc, vc, graph
 
     # BF16-cache comparison on the same workload (attention only, L2 flushed)
@@ -455,13 +469,17 @@ def run_ours(args):
                        "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3",
                        "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
                        "split_combine": combine,
-                       "step": ("kvq_tag_check, then kvq_decode_attn_append" if args.fused_append
+                       "step": ("kvq_decode_step (tag check, append and attention in one launch)"
+                                if args.one_launch else
+                                "kvq_tag_check, then kvq_decode_attn_append" if args.fused_append
                                 else "kvq_tag_check_append, then kvq_decode_attn"),
                        "l2": "flushed before every timed step (512 MiB write)",
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": round(agg["tokens_per_s"], 1),
             "hbm_frac_of_measured": round(kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
-            "kernel_us": ({"tag_check": round(pre_ms * 1e3, 2),
+            "kernel_us": ({"decode_step (tag check + append + split + fused combine)": round(attn_ms * 1e3, 2)}
+                          if args.one_launch else
+                          {"tag_check": round(pre_ms * 1e3, 2),
                            "decode_attn_append (append + split + fused combine)": round(attn_ms * 1e3, 2)}
                           if args.fused_append else
                           {"tag_check_append": round(pre_ms * 1e3, 2),
@@ -473,7 +491,7 @@ def run_ours(args):
             "e2e": {"value": round(kv_bytes / (e2e_ms_mean / 1e3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms_mean, 4), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": (1 if args.one_launch else 2) * args.steps,
             "bf16_cache": bf16_line,
             "steady_state_graph": steady,
             "clocks": sampler.summary(t_wall0, t_wall1),
@@ -715,6 +733,8 @@ def main():
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="churn: replay the step as a CUDA graph")
+    ap.add_argument("--one-launch", action="store_true",
+                    help="decode workloads: the whole step as one kvq_decode_step launch")
     ap.add_argument("--fused-append", action="store_true",
                     help="step = tag check, then decode attention with the append fused in")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -11,6 +11,7 @@ missing the calls raise.
     kvq_decode_attn(...)    split-K paged decode attention + LSE combine
     kvq_decode_plan(...)    split / workspace sizes for kvq_decode_attn
     kvq_decode_attn_append(...), kvq_tag_check_append(...)   fused forms
+    kvq_decode_step(...)    tag check + append + attention of a decode step, one launch
     kvq_amax_scales(...), kvq_quantize_pages(...)            prefill -> decode handoff
     kvq_w4a16_gemm(...)     INT4 weight-only product for decode
 """
@@ -66,6 +67,8 @@ _SIGS = {
                         "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_decode_attn_append": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
                                "p", "p", "p", "p", "i32", "p", "size", "i32", "p"],
+    "kvq_decode_step": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "p", "p", "p",
+                        "f32", "p", "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_w4a16_plan": ["i32", "i32", "i32", "i32", "p"],
     "kvq_w4a16_gemm": ["p", "p", "p", "i32", "i32", "i32", "p", "i32", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
@@ -283,6 +286,40 @@ def kvq_decode_attn_append(desc, q, k_cache, v_cache, k_scale, v_scale, block_ta
         ctypes.c_float(softmax_scale), _ptr(abort_flags), _ptr(k_new), _ptr(v_new), _ptr(out),
         out_dtype, _ptr(workspace), ws_bytes, num_splits, _stream(stream))
     _check("kvq_decode_attn_append", st)
+    return out
+
+
+def kvq_decode_step(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, expected_tags,
+                    page_tags, abort_flags, softmax_scale, k_new, v_new, out, workspace, num_splits=0,
+                    stream=None):
+    """A whole decode step in one launch: the tag check of every request
+    (flags written into ``abort_flags``, uint8 [B]), then, for each request
+    that passed, the append of its new token at seq_lens[r] - 1 and paged
+    decode attention into ``out``.  The same results as kvq_tag_check
+    followed by kvq_decode_attn_append."""
+    import torch
+    B, Hq, D = q.shape
+    maxp = block_table.shape[1]
+    _expect(q, torch.bfloat16, (B, Hq, desc.head_dim), "q")
+    _expect(block_table, torch.int32, None, "block_table")
+    _expect(seq_lens, torch.int32, (B,), "seq_lens")
+    if expected_tags.element_size() != 4 or tuple(expected_tags.shape) != (B, maxp):
+        raise ValueError("expected_tags: expected 32-bit tags [B][max_pages]")
+    if page_tags.element_size() != 4 or tuple(page_tags.shape) != (desc.num_pages,):
+        raise ValueError("page_tags: expected 32-bit tags [num_pages]")
+    _expect(abort_flags, torch.uint8, (B,), "abort_flags")
+    _expect(k_new, torch.bfloat16, (B, desc.num_kv_heads, desc.head_dim), "k_new")
+    _expect(v_new, torch.bfloat16, (B, desc.num_kv_heads, desc.head_dim), "v_new")
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("out: expected bf16 or fp32 [B][Hq][D]")
+    out_dtype = KVQ_OUT_FP32 if out.dtype == torch.float32 else KVQ_OUT_BF16
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kvq_decode_step(
+        ctypes.byref(desc.c()), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), maxp, _ptr(seq_lens), _ptr(expected_tags), _ptr(page_tags),
+        _ptr(abort_flags), ctypes.c_float(softmax_scale), _ptr(k_new), _ptr(v_new), _ptr(out),
+        out_dtype, _ptr(workspace), ws_bytes, num_splits, _stream(stream))
+    _check("kvq_decode_step", st)
     return out
 
 

@@ -530,6 +530,37 @@ kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void *q, int
     return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_decode_step(const kvq_cache_desc *desc, const void *q, int32_t batch, int32_t num_q_heads,
+                           void *k_cache, void *v_cache, const float *k_scale, const float *v_scale,
+                           const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                           const uint32_t *expected_tags, const uint32_t *page_tags, uint8_t *abort_flags,
+                           float softmax_scale, const void *k_new, const void *v_new, void *out,
+                           int32_t out_dtype, void *workspace, size_t workspace_bytes, int32_t num_splits,
+                           kvq_stream_t stream)
+{
+    DecodeCall call;
+    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                   block_table, max_pages_per_seq, seq_lens, softmax_scale, nullptr, out,
+                                   out_dtype, workspace, workspace_bytes, num_splits, &call);
+    if (st != KVQ_OK || batch == 0)
+        return st;
+    if (!expected_tags || !page_tags || !abort_flags)
+        return KVQ_ERR_INVALID_ARG;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return KVQ_ERR_INVALID_ARG;
+    call.args.k_new = k_new;
+    call.args.v_new = v_new;
+    call.args.k_cache = k_cache;
+    call.args.v_cache = v_cache;
+    call.args.expected_tags = expected_tags;
+    call.args.page_tags = page_tags;
+    call.args.abort_out = abort_flags;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
+        return KVQ_ERR_CUDA;
+    return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_device_error(uint32_t *bits, int32_t clear)
 {
     uint32_t a = 0, b = 0;

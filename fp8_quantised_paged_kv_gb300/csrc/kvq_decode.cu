@@ -48,6 +48,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // give up on a copy after ~1 s
 constexpr int kPrefetchTokens = 256;             // per split, requested into L2 before the wait
+constexpr int kStepTagUnroll = 8;               // in-launch tag check: entries per thread per pass
 
 template <bool kBf16Cache>
 struct Tile {
@@ -338,9 +339,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         ids[k] = i < span ? __ldg(bt + i) : -1;
     }
     const int64_t len = a.seq_lens[b];
-    const bool aborted = a.abort_flags != nullptr && a.abort_flags[b] != 0;
+    // kvq_decode_step: every CTA of the request runs the request's tag check
+    // itself (all reach the same verdict from the same entries), after its
+    // first copies are under way and before it writes the cache or uses what
+    // it reads; split 0 of KV head 0 reports the verdict.
+    const bool step_check = a.expected_tags != nullptr;
+    const bool reporter = step_check && split == 0 && kvh == 0 && threadIdx.x == 0;
+    const bool aborted = !step_check && a.abort_flags != nullptr && a.abort_flags[b] != 0;
     const int64_t cap = static_cast<int64_t>(a.max_pages_per_seq) * ps;
     const bool zero_request = aborted || len <= 0 || len > cap;
+    if (reporter && zero_request)                          // the check's verdict without a look:
+        a.abort_out[b] = len > cap ? 1 : 0;                // too long fails, empty passes
     const int nsplit = zero_request ? 1 : static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
     float *part = reinterpret_cast<float *>(smem) + kScratchOffset;   // cluster partial
     if constexpr (kCluster) {
@@ -388,6 +397,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     int it_new = -1;
     using NewRow = std::conditional_t<kBf16Cache, uint2, uint32_t>;   // a lane's part of the row
     NewRow new_k{}, new_v{};
+    int64_t new_row = -1;                                  // cache row of the new token
     if (a.k_new != nullptr && split == nsplit - 1) {
         const int64_t tpos = len - 1;
         const int c_last = static_cast<int>((tpos - t0) / kChunkTokens);
@@ -397,22 +407,33 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             const int64_t src = (static_cast<int64_t>(b) * a.num_kv_heads + kvh) * kHeadDim + 4 * lane;
             const uint2 xk = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.k_new) + src);
             const uint2 xv = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.v_new) + src);
-            const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + tpos % ps;
+            new_row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + tpos % ps;
             if constexpr (kBf16Cache) {
                 new_k = xk;
                 new_v = xv;
-                *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.k_cache) + row * 256 + 8 * lane) = xk;
-                *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.v_cache) + row * 256 + 8 * lane) = xv;
             } else {
                 new_k = encode4_e4m3(xk.x, xk.y, a.k_scale[kvh]);
                 new_v = encode4_e4m3(xv.x, xv.y, a.v_scale[kvh]);
-                *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.k_cache) + row * 128 + 4 * lane) = new_k;
-                *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.v_cache) + row * 128 + 4 * lane) = new_v;
             }
         }
     }
+    auto write_new = [&]() {
+        if (new_row < 0)
+            return;
+        if constexpr (kBf16Cache) {
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.k_cache) + new_row * 256 + 8 * lane) = new_k;
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.v_cache) + new_row * 256 + 8 * lane) = new_v;
+        } else {
+            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.k_cache) + new_row * 128 + 4 * lane) = new_k;
+            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.v_cache) + new_row * 128 + 4 * lane) = new_v;
+        }
+    };
+    if (!step_check)                                       // kvq_decode_step writes after its check
+        write_new();
 
     if (bad) {
+        if (reporter)                                      // a listed page is out of range
+            a.abort_out[b] = 1;
         if constexpr (kCluster)
             cluster_finish(a, b, kvh, kPartialInvalid, part);
         else
@@ -455,10 +476,32 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         }
     };
 
-    if (lane == 0) {
-        const int pro = my_chunks < T::kStages ? my_chunks : T::kStages;
+    const int pro = my_chunks < T::kStages ? my_chunks : T::kStages;
+    if (lane == 0)
         for (int it = 0; it < pro; ++it)
             issue(it);
+
+    if (step_check) {
+        const bool stale = tag_check_request<kStepTagUnroll>(a.block_table, a.expected_tags, a.seq_lens,
+                                                             a.page_tags, a.max_pages_per_seq, ps,
+                                                             a.num_pages, b);
+        if (reporter)
+            a.abort_out[b] = stale ? 1 : 0;
+        if (stale) {
+            // let the copies already issued land (bounded waits) before the
+            // shared memory is reused, then give the split up like a bad page
+            if (lane == 0)
+                for (int it = 0; it < pro; ++it)
+                    if (!mbar_wait_bounded(&my_full[it], 0, kWaitLimitNs))
+                        atomicOr(&g_device_error, 1u);
+            __syncthreads();
+            if constexpr (kCluster)
+                cluster_finish(a, b, kvh, kPartialInvalid, part);
+            else
+                drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
+            return;
+        }
+        write_new();
     }
 
     // Query fragments (mma B operand): lane (gq, tq) holds query head gq of

@@ -97,6 +97,9 @@ struct DecodeArgs {
     void *k_cache, *v_cache;         // fused append: the caches the token is written to
     int32_t cluster;                 // 0: combine through memory; else the splits of a
                                      // (request, KV head) form one cluster of max_splits CTAs
+    const uint32_t *expected_tags;   // in-launch tag check (kvq_decode_step): [B][max_pages],
+    const uint32_t *page_tags;       // [num_pages] and the flags written, [B]; else null and
+    uint8_t *abort_out;              // abort_flags (if any) is read instead
     float qk_scale_log2;             // softmax_scale * log2(e)
     bool out_fp32, bf16_cache;
 };

@@ -291,6 +291,39 @@ KVQ_API kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void
                                   size_t workspace_bytes, int32_t num_splits, kvq_stream_t stream);
 
 /*
+ * kvq_decode_step -- one decode step in one launch: the tag check of every
+ * request (page-3 article: check before the cache is read; page-2 summary,
+ * section "KV Cache 完整性检查"), then, for each request that passed, the
+ * append of its new token and paged decode attention over the FP8 (or BF16)
+ * cache (page-1 article, section "量化KV缓存").
+ *
+ *   expected_tags  uint32 [B][max_pages_per_seq]: the tag request r expects
+ *                  for each of its pages, as in kvq_tag_check.
+ *   page_tags      uint32 [desc->num_pages]: the live tag of every page.
+ *   abort_flags    uint8 [B] OUTPUT: 1 where the check failed, else 0 --
+ *                  the flags kvq_tag_check writes.
+ *   Every other argument as in kvq_decode_attn_append (the abort_flags
+ *   input of that call is this call's output).
+ * Results equal kvq_tag_check followed by kvq_decode_attn_append with its
+ * flags, bit for bit: flags, cache writes and outputs.  Every CTA of a
+ * request repeats the request's check (its block-table row, expected tags
+ * and the live tags they name: 12 bytes per page) before it writes the
+ * cache or uses what it reads; split 0 of KV head 0 writes the flag.  A
+ * failed request gets zeros and no write.  Null expected_tags, page_tags or
+ * abort_flags is KVQ_ERR_INVALID_ARG; everything else is checked as in
+ * kvq_decode_attn_append.
+ */
+KVQ_API kvq_status kvq_decode_step(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                   int32_t num_q_heads, void *k_cache, void *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, int32_t max_pages_per_seq,
+                                   const int32_t *seq_lens, const uint32_t *expected_tags,
+                                   const uint32_t *page_tags, uint8_t *abort_flags,
+                                   float softmax_scale, const void *k_new, const void *v_new,
+                                   void *out, int32_t out_dtype, void *workspace,
+                                   size_t workspace_bytes, int32_t num_splits, kvq_stream_t stream);
+
+/*
  * kvq_w4a16_plan / kvq_w4a16_gemm -- INT4 weight-only product for decode
  * (blog post "Smaller, faster, safer", page-1 mirror section "压缩模型权重":
  * weights compressed from FP8 to 4-bit integers for decode, which streams

@@ -126,6 +126,15 @@ class DeviceWorkload:
                                  self.k_scale, self.v_scale, self.k_cache, self.v_cache,
                                  self.abort, stream)
 
+    def decode_step(self, out, workspace, num_splits=0, stream=None):
+        """The whole step in one launch (kvq_decode_step): tag check, append
+        of each passing request's token at seq_lens[r] - 1, attention."""
+        kvq.kvq_decode_step(self.desc, self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                            self.block_table, self.seq_lens, self.expected_tags, self.page_tags,
+                            self.abort, self.w.softmax_scale, self.k_new, self.v_new, out, workspace,
+                            num_splits, stream)
+        return out
+
     def step(self, out, workspace, num_splits=0, stream=None, fused=True):
         """tag check -> append (skips aborted) -> attention (zeros for aborted).
         fused: the first two as one launch (kvq_tag_check_append)."""
