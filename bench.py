@@ -1,11 +1,13 @@
 """Benchmark of the FP8 paged-KV decode step on GB300.
 
-One step = one decode step of one layer of the workload: the batched tag
-check with the FP8 quantise-on-append of each request's new token (one
-launch, kvq_tag_check_append), then the split-K paged decode attention with
-its log-sum-exp combine fused in (one launch, kvq_decode_attn).  Default
-workload: 8 requests x 8,193 tokens, GQA 64/8, head_dim 128, page 16, FP8
-e4m3 cache with per-head scales, K/V ~ N(0,1) with 1 % outliers x20.
+One step = one decode step of one layer of the workload: the tag check of
+every request, the FP8 quantise-on-append of each passing request's new
+token, and the split-K paged decode attention with its log-sum-exp combine,
+all in one launch (kvq_decode_step).  --two-launch times the same step as
+kvq_tag_check_append then kvq_decode_attn, --fused-append as kvq_tag_check
+then kvq_decode_attn_append.  Default workload: 8 requests x 8,193 tokens,
+GQA 64/8, head_dim 128, page 16, FP8 e4m3 cache with per-head scales, K/V ~
+N(0,1) with 1 % outliers x20.
 
 Prints one JSON line.  `value` is KV-read GB/s of the whole step (algorithmic
 FP8 K+V bytes of all attended tokens / device time of the step); tokens/s,
@@ -277,10 +279,12 @@ def run_ours(args):
                "cluster (distributed shared memory)" if ws_bytes == counter_bytes else
                "workspace (last-arriving split)")
 
+    one_launch = not (args.two_launch or args.fused_append)
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        if args.one_launch:                    # tag check + append + attention, one launch
+        if one_launch:                    # tag check + append + attention, one launch
             if ev is not None:
                 ev[1].record(stream)
             dw.decode_step(out, ws, args.num_splits, stream)
@@ -389,7 +393,7 @@ def run_ours(args):
         vc = [dw.v_cache.clone() for _ in range(R)]
         def steady_steps(st):
             for r in range(R):
-                if args.one_launch:
+                if one_launch:
                     kvq.kvq_decode_step(dw.desc, dw.q, kc[r], vc[r], dw.k_scale, dw.v_scale,
                                         dw.block_table, dw.seq_lens, dw.expected_tags, dw.page_tags,
                                         dw.abort, w.softmax_scale, dw.k_new, dw.v_new, out, ws,
@@ -425,7 +429,7 @@ def run_ours(args):
                   "us_per_step": round(per_step_ms * 1e3, 3),
                   "kv_gbs": round(kv_bytes / (per_step_ms / 1e3) / 1e9, 2),
                   "how": ("one CUDA graph of R back-to-back steps (" +
-                          ("kvq_decode_step" if args.one_launch else "tag check + append, then decode") +
+                          ("kvq_decode_step" if one_launch else "tag check + append, then decode") +
                           "), step r on cache copy r; L2 flushed before each replay")}
         del kc, vc, graph
 
@@ -470,7 +474,7 @@ def run_ours(args):
                        "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
                        "split_combine": combine,
                        "step": ("kvq_decode_step (tag check, append and attention in one launch)"
-                                if args.one_launch else
+                                if one_launch else
                                 "kvq_tag_check, then kvq_decode_attn_append" if args.fused_append
                                 else "kvq_tag_check_append, then kvq_decode_attn"),
                        "l2": "flushed before every timed step (512 MiB write)",
@@ -478,7 +482,7 @@ def run_ours(args):
             "tokens_per_s": round(agg["tokens_per_s"], 1),
             "hbm_frac_of_measured": round(kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
             "kernel_us": ({"decode_step (tag check + append + split + fused combine)": round(attn_ms * 1e3, 2)}
-                          if args.one_launch else
+                          if one_launch else
                           {"tag_check": round(pre_ms * 1e3, 2),
                            "decode_attn_append (append + split + fused combine)": round(attn_ms * 1e3, 2)}
                           if args.fused_append else
@@ -491,7 +495,7 @@ def run_ours(args):
             "e2e": {"value": round(kv_bytes / (e2e_ms_mean / 1e3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms_mean, 4), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": (1 if args.one_launch else 2) * args.steps,
+            "gpu_launches": (1 if one_launch else 2) * args.steps,
             "bf16_cache": bf16_line,
             "steady_state_graph": steady,
             "clocks": sampler.summary(t_wall0, t_wall1),
@@ -733,8 +737,9 @@ def main():
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="churn: replay the step as a CUDA graph")
-    ap.add_argument("--one-launch", action="store_true",
-                    help="decode workloads: the whole step as one kvq_decode_step launch")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="decode workloads: the step as kvq_tag_check_append, then kvq_decode_attn "
+                         "(default: one kvq_decode_step launch)")
     ap.add_argument("--fused-append", action="store_true",
                     help="step = tag check, then decode attention with the append fused in")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

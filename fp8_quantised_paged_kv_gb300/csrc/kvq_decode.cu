@@ -48,7 +48,11 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // give up on a copy after ~1 s
 constexpr int kPrefetchTokens = 256;             // per split, requested into L2 before the wait
-constexpr int kStepTagUnroll = 8;               // in-launch tag check: entries per thread per pass
+// Published lse of a split that has no result: both are NaN, so the combine
+// zeroes the request either way; the payload tells a failed tag check (the
+// request is aborted and its new token not written) from a copy timeout.
+constexpr uint32_t kLseInvalid = 0x7FC00000u;
+constexpr uint32_t kLseStale = 0x7FC0A5A5u;
 
 template <bool kBf16Cache>
 struct Tile {
@@ -120,6 +124,37 @@ static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kHeadDim) * 4 <= Tile<fa
 //   M = max_s lse_s,  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
 // for every query head of the group at once, writes the output (zeros for
 // a head if any split was invalid) and resets the counter.
+// kvq_decode_step, once per (request, KV head), by the CTA that knows the
+// verdict of all the request's splits: KV head 0 writes the abort flag, and
+// a request that passed gets its new token written for this KV head (the
+// codes kvq_append writes).  A split holding the token has already patched
+// them into its own tile, and no other CTA of this launch reads that row.
+__device__ void finish_step(const DecodeArgs &a, int b, int kvh, bool stale)
+{
+    if (kvh == 0 && threadIdx.x == 0)
+        a.abort_out[b] = stale ? 1 : 0;
+    if (stale || threadIdx.x >= 32)
+        return;
+    const int lane = threadIdx.x;
+    const int64_t tpos = static_cast<int64_t>(a.seq_lens[b]) - 1;     // > 0: the request was not empty
+    const int32_t page = a.block_table[static_cast<int64_t>(b) * a.max_pages_per_seq + tpos / a.page_size];
+    if (page < 0 || page >= a.num_pages)                                 // excluded by the check
+        return;
+    const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * a.page_size + tpos % a.page_size;
+    const int64_t src = (static_cast<int64_t>(b) * a.num_kv_heads + kvh) * kHeadDim + 4 * lane;
+    const uint2 xk = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.k_new) + src);
+    const uint2 xv = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.v_new) + src);
+    if (a.bf16_cache) {
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.k_cache) + row * 256 + 8 * lane) = xk;
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.v_cache) + row * 256 + 8 * lane) = xv;
+    } else {
+        *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.k_cache) + row * 128 + 4 * lane) =
+            encode4_e4m3(xk.x, xk.y, a.k_scale[kvh]);
+        *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.v_cache) + row * 128 + 4 * lane) =
+            encode4_e4m3(xv.x, xv.y, a.v_scale[kvh]);
+    }
+}
+
 __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsplit, float *scratch)
 {
     __shared__ int s_last;
@@ -194,6 +229,17 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
                 store_out(a.out, (bh0 + h) * kHeadDim + d, s_tot[h] > 0.f ? acc[h] / s_tot[h] : 0.f,
                           a.out_fp32);
     }
+    if (a.expected_tags != nullptr) {        // kvq_decode_step: the request's verdict
+        __shared__ int s_stale_any;
+        if (threadIdx.x == 0) {
+            int any = 0;
+            for (int sp = 0; sp < n; ++sp)
+                any |= __float_as_uint(__ldcg(a.ws_lse + bh0 * a.max_splits + sp)) == kLseStale;
+            s_stale_any = any;
+        }
+        __syncthreads();
+        finish_step(a, b, kvh, s_stale_any != 0);
+    }
     if (threadIdx.x == 0)
         *counter = 0;                        // ready for the next call
 }
@@ -201,23 +247,26 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
 // A split that cannot produce a result (invalid page id, or a copy that
 // timed out): a single-split request gets zeros; otherwise the split
 // publishes an invalid (NaN) lse so the combine zeroes the request.
-__device__ void drop_split(const DecodeArgs &a, int b, int kvh, int split, int nsplit, float *smem)
+__device__ void drop_split(const DecodeArgs &a, int b, int kvh, int split, int nsplit, float *smem,
+                           uint32_t lse_bits = kLseInvalid)
 {
     const int hq0 = kvh * a.group;
     if (nsplit == 1) {
         for (int i = threadIdx.x; i < a.group * kHeadDim; i += kThreads)
             store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + hq0) * kHeadDim + i, 0.f,
                       a.out_fp32);
+        if (a.expected_tags != nullptr)
+            finish_step(a, b, kvh, lse_bits == kLseStale);
         return;
     }
     if (threadIdx.x < a.group)
         a.ws_lse[(static_cast<int64_t>(b) * a.num_q_heads + hq0 + threadIdx.x) * a.max_splits + split] =
-            __int_as_float(0x7FC00000);
+            __uint_as_float(lse_bits);
     publish_and_combine(a, b, kvh, nsplit, smem + kScratchOffset);
 }
 
 // What a split contributes to the cluster form of the combine.
-enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2 };
+enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPartialStale = 3 };
 
 // Cluster form of the combine, used when the splits of each (request, KV
 // head) are the CTAs of one thread-block cluster (every split resident at
@@ -229,11 +278,15 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2 };
 // distributed shared memory:
 //   M = max_s lse_s,  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).
 // A second barrier keeps every CTA's shared memory alive until its peers
-// have read it.  Every CTA of the cluster calls this exactly once.
-__device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part)
+// have read it.  Every CTA of the cluster calls this exactly once, with the
+// same `finisher`: for kvq_decode_step the rank that then reads every peer's
+// verdict and finishes the step (finish_step), else -1.
+__device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part,
+                               int finisher)
 {
     if (status != kPartialOk && threadIdx.x < kMaxGroup)
-        part[threadIdx.x] = status == kPartialEmpty ? -INFINITY : __int_as_float(0x7FC00000);
+        part[threadIdx.x] = status == kPartialEmpty ? -INFINITY
+                            : __uint_as_float(status == kPartialStale ? kLseStale : kLseInvalid);
     cluster_sync();
     const int g = a.group, n = a.max_splits;
     const int rank = static_cast<int>(cluster_ctarank());
@@ -270,6 +323,13 @@ __device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
         store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * kHeadDim + d,
                   (bad || !(sum > 0.f)) ? 0.f : acc / sum, a.out_fp32);
     }
+    if (rank == finisher) {                  // every peer's head-0 lse carries its verdict
+        bool stale = false;
+        for (int sp = 0; sp < n; ++sp)
+            stale |= __float_as_uint(ld_shared_cluster_f32(map_shared_rank(base, static_cast<uint32_t>(sp)))) ==
+                     kLseStale;
+        finish_step(a, b, kvh, stale);
+    }
     cluster_sync();
 }
 
@@ -285,6 +345,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
     int32_t *page_list = reinterpret_cast<int32_t *>(full + kWarps * T::kStages);
     __shared__ int s_failed;
+    __shared__ int s_stale;                                // kvq_decode_step: a page of this split failed
 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -339,10 +400,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         ids[k] = i < span ? __ldg(bt + i) : -1;
     }
     const int64_t len = a.seq_lens[b];
-    // kvq_decode_step: every CTA of the request runs the request's tag check
-    // itself (all reach the same verdict from the same entries), after its
-    // first copies are under way and before it writes the cache or uses what
-    // it reads; split 0 of KV head 0 reports the verdict.
+    // kvq_decode_step: each split checks the tags of its own pages (together
+    // the request's used entries) while its first copies fly, and publishes
+    // a failure with its partial; the CTA that sees every split's partial
+    // (finish_step) writes the flag and, if the request passed, its new
+    // token.  A request without tokens to check is decided here.
     const bool step_check = a.expected_tags != nullptr;
     const bool reporter = step_check && split == 0 && kvh == 0 && threadIdx.x == 0;
     const bool aborted = !step_check && a.abort_flags != nullptr && a.abort_flags[b] != 0;
@@ -352,9 +414,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         a.abort_out[b] = len > cap ? 1 : 0;                // too long fails, empty passes
     const int nsplit = zero_request ? 1 : static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
     float *part = reinterpret_cast<float *>(smem) + kScratchOffset;   // cluster partial
+    // kvq_decode_step: the split that finishes the step of a request with
+    // tokens (the cluster's last split)
+    const int finisher = step_check && !zero_request ? nsplit - 1 : -1;
     if constexpr (kCluster) {
         if (zero_request || split >= nsplit) {             // no tokens: weight 0
-            cluster_finish(a, b, kvh, kPartialEmpty, part);
+            cluster_finish(a, b, kvh, kPartialEmpty, part, finisher);
             return;
         }
     }
@@ -383,6 +448,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     if (threadIdx.x == 0) {
         s_failed = 0;
+        s_stale = 0;
         for (int i = 0; i < kWarps * T::kStages; ++i)
             mbar_init(&full[i], 1);
         fence_mbar_init();
@@ -428,16 +494,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(a.v_cache) + new_row * 128 + 4 * lane) = new_v;
         }
     };
-    if (!step_check)                                       // kvq_decode_step writes after its check
+    if (!step_check)                                       // kvq_decode_step: finish_step writes it
         write_new();
 
-    if (bad) {
-        if (reporter)                                      // a listed page is out of range
-            a.abort_out[b] = 1;
+    if (bad) {                                             // for kvq_decode_step a failed check
         if constexpr (kCluster)
-            cluster_finish(a, b, kvh, kPartialInvalid, part);
+            cluster_finish(a, b, kvh, step_check ? kPartialStale : kPartialInvalid, part, finisher);
         else
-            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
+            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem),
+                       step_check ? kLseStale : kLseInvalid);
         return;
     }
 
@@ -482,26 +547,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             issue(it);
 
     if (step_check) {
-        const bool stale = tag_check_request<kStepTagUnroll>(a.block_table, a.expected_tags, a.seq_lens,
-                                                             a.page_tags, a.max_pages_per_seq, ps,
-                                                             a.num_pages, b);
-        if (reporter)
-            a.abort_out[b] = stale ? 1 : 0;
-        if (stale) {
-            // let the copies already issued land (bounded waits) before the
-            // shared memory is reused, then give the split up like a bad page
-            if (lane == 0)
-                for (int it = 0; it < pro; ++it)
-                    if (!mbar_wait_bounded(&my_full[it], 0, kWaitLimitNs))
-                        atomicOr(&g_device_error, 1u);
-            __syncthreads();
-            if constexpr (kCluster)
-                cluster_finish(a, b, kvh, kPartialInvalid, part);
-            else
-                drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
-            return;
+        // kvq_decode_step: this split's share of the tag check, its own pages
+        // (whose ids are in range here), while the first copies fly.  The
+        // split attends regardless; a failure only changes what it publishes.
+        const uint32_t *want = a.expected_tags + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
+        bool stale = false;
+#pragma unroll
+        for (int k = 0; k < kIdsPerThread; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            if (i < n_pages)
+                stale |= __ldg(a.page_tags + page_list[i]) != __ldg(want + i);
         }
-        write_new();
+        if (stale)
+            s_stale = 1;
     }
 
     // Query fragments (mma B operand): lane (gq, tq) holds query head gq of
@@ -755,11 +813,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             mbar_wait_bounded(&my_full[j % T::kStages], (j / T::kStages) & 1, kWaitLimitNs);
     }
     __syncthreads();
-    if (s_failed) {
+    if (s_stale || s_failed) {                             // a failed check outranks a timeout
         if constexpr (kCluster)
-            cluster_finish(a, b, kvh, kPartialInvalid, part);
+            cluster_finish(a, b, kvh, s_stale ? kPartialStale : kPartialInvalid, part, finisher);
         else
-            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem));
+            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem),
+                       s_stale ? kLseStale : kLseInvalid);
         return;
     }
 
@@ -828,10 +887,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 a.ws_lse[bh * a.max_splits + split] = sm_t[kMaxGroup + h];
         }
     }
-    if constexpr (kCluster)
-        cluster_finish(a, b, kvh, kPartialOk, part);
-    else if (nsplit > 1)
+    if constexpr (kCluster) {
+        cluster_finish(a, b, kvh, kPartialOk, part, finisher);
+    } else if (nsplit > 1) {
         publish_and_combine(a, b, kvh, nsplit, reinterpret_cast<float *>(smem) + kScratchOffset);
+    } else if (step_check) {                               // one split: its own verdict
+        finish_step(a, b, kvh, false);
+    }
 }
 
 template <bool kBf16, bool kPrecise, bool kCluster>

@@ -305,13 +305,13 @@ KVQ_API kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void
  *   Every other argument as in kvq_decode_attn_append (the abort_flags
  *   input of that call is this call's output).
  * Results equal kvq_tag_check followed by kvq_decode_attn_append with its
- * flags, bit for bit: flags, cache writes and outputs.  Every CTA of a
- * request repeats the request's check (its block-table row, expected tags
- * and the live tags they name: 12 bytes per page) before it writes the
- * cache or uses what it reads; split 0 of KV head 0 writes the flag.  A
- * failed request gets zeros and no write.  Null expected_tags, page_tags or
- * abort_flags is KVQ_ERR_INVALID_ARG; everything else is checked as in
- * kvq_decode_attn_append.
+ * flags, bit for bit: flags, cache writes and outputs.  Each split of the
+ * attention checks the entries of its own pages while it streams them; the
+ * CTA that combines a request's splits (per KV head) learns the verdict,
+ * and only then is the flag written (by KV head 0) and, if the request
+ * passed, its new token.  A failed request gets zeros and no write.  Null
+ * expected_tags, page_tags or abort_flags is KVQ_ERR_INVALID_ARG;
+ * everything else is checked as in kvq_decode_attn_append.
  */
 KVQ_API kvq_status kvq_decode_step(const kvq_cache_desc *desc, const void *q, int32_t batch,
                                    int32_t num_q_heads, void *k_cache, void *v_cache,
