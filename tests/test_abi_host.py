@@ -86,6 +86,33 @@ def test_calls_with_null_pointers_fail_on_the_host():
     assert lib.kvq_tag_check(None, None, None, 0, 8, 16, None, 64, None, None) == 0
 
 
+def test_decode_step_argument_checks_on_the_host():
+    """kvq_decode_step: null tensors, a missing tag array or output flags, and
+    a short workspace are reported before anything reaches a GPU."""
+    lib = kvq.load()
+    desc = kvq.CacheDesc(4104, 16, 8).c()
+    p = ctypes.c_void_p(0x10000)
+    f = ctypes.c_float(0.1)
+    st = lib.kvq_decode_step(ctypes.byref(desc), None, 2, 16, None, None, None, None, None, 8, None,
+                             None, None, None, f, None, None, None, 0, None, 0, 0, None)
+    assert st == 1
+    big = 1 << 30
+    for missing in range(3):                     # expected tags, live tags, flags
+        tags = [p, p, p]
+        tags[missing] = None
+        st = lib.kvq_decode_step(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p, *tags, f, p, p, p,
+                                 0, p, big, 0, None)
+        assert st == 1
+    st = lib.kvq_decode_step(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p, p, p, p, f, None, p, p,
+                             0, p, big, 0, None)
+    assert st == 1                               # no new token
+    st = lib.kvq_decode_step(ctypes.byref(desc), p, 8, 64, p, p, p, p, p, 513, p, p, p, p, f, p, p, p,
+                             0, p, 16, 0, None)
+    assert st == 3                               # workspace too small
+    assert lib.kvq_decode_step(ctypes.byref(desc), p, 0, 64, p, p, p, p, p, 513, p, p, p, p, f, p, p, p,
+                               0, p, big, 0, None) == 0    # empty batch: nothing to do
+
+
 def test_misaligned_pointer_rejected():
     lib = kvq.load()
     desc = kvq.CacheDesc(64, 16, 8).c()
