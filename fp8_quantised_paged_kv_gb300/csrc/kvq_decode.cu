@@ -62,7 +62,9 @@ struct Tile {
     static constexpr int kStageBytes = 2 * kBytes;
     static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRingBytes +
-                                      kWarps * kStages * 8 /* barriers */ + kMaxPageList * 4 + 16;
+                                      kWarps * kStages * 8 /* barriers */ + kMaxPageList * 4 +
+                                      2 * kMaxPageList * 4 /* tags of the split's pages */ +
+                                      512 /* the new token's K and V row */ + 16;
 };
 
 // Byte offset of 16-byte chunk `c` of 128-byte line `line` in a tile written
@@ -279,11 +281,13 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPa
 //   M = max_s lse_s,  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).
 // A second barrier keeps every CTA's shared memory alive until its peers
 // have read it.  Every CTA of the cluster calls this exactly once, with the
-// same `finisher`: for kvq_decode_step the rank that then reads every peer's
-// verdict and finishes the step (finish_step), else -1.
-__device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part,
+// same `finisher`: for kvq_decode_step the rank that reads every peer's
+// verdict, else -1.  Returns, on the finisher, whether any split of the
+// request failed its tag check (false elsewhere).
+__device__ bool cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part,
                                int finisher)
 {
+    __shared__ int s_any_stale;
     if (status != kPartialOk && threadIdx.x < kMaxGroup)
         part[threadIdx.x] = status == kPartialEmpty ? -INFINITY
                             : __uint_as_float(status == kPartialStale ? kLseStale : kLseInvalid);
@@ -291,6 +295,13 @@ __device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
     const int g = a.group, n = a.max_splits;
     const int rank = static_cast<int>(cluster_ctarank());
     const uint32_t base = smem_addr(part);
+    if (rank == finisher && threadIdx.x == 0) {            // every peer's head-0 lse carries its verdict
+        int stale = 0;
+        for (int sp = 0; sp < n; ++sp)
+            stale |= __float_as_uint(ld_shared_cluster_f32(map_shared_rank(base, static_cast<uint32_t>(sp)))) ==
+                     kLseStale;
+        s_any_stale = stale;
+    }
     for (int h = rank; h < g; h += n)
     for (int d = threadIdx.x; d < kHeadDim; d += kThreads) {
         float lse[kMaxCluster], ov[kMaxCluster];
@@ -323,14 +334,8 @@ __device__ void cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
         store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * kHeadDim + d,
                   (bad || !(sum > 0.f)) ? 0.f : acc / sum, a.out_fp32);
     }
-    if (rank == finisher) {                  // every peer's head-0 lse carries its verdict
-        bool stale = false;
-        for (int sp = 0; sp < n; ++sp)
-            stale |= __float_as_uint(ld_shared_cluster_f32(map_shared_rank(base, static_cast<uint32_t>(sp)))) ==
-                     kLseStale;
-        finish_step(a, b, kvh, stale);
-    }
-    cluster_sync();
+    cluster_sync();                          // also orders s_any_stale within the CTA
+    return rank == finisher && s_any_stale != 0;
 }
 
 template <bool kBf16Cache, bool kPreciseP, bool kCluster>
@@ -344,6 +349,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
     int32_t *page_list = reinterpret_cast<int32_t *>(full + kWarps * T::kStages);
+    uint32_t *tag_live = reinterpret_cast<uint32_t *>(page_list + kMaxPageList);   // kvq_decode_step:
+    uint32_t *tag_want = tag_live + kMaxPageList;                                  // the split's tags
+    uint8_t *new_tok = reinterpret_cast<uint8_t *>(tag_want + kMaxPageList);       // [K row][V row]
     __shared__ int s_failed;
     __shared__ int s_stale;                                // kvq_decode_step: a page of this split failed
 
@@ -481,8 +489,29 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 new_k = encode4_e4m3(xk.x, xk.y, a.k_scale[kvh]);
                 new_v = encode4_e4m3(xv.x, xv.y, a.v_scale[kvh]);
             }
+            if (step_check) {                              // kept for the end of the step
+                reinterpret_cast<NewRow *>(new_tok)[lane] = new_k;
+                reinterpret_cast<NewRow *>(new_tok + T::kRowBytes)[lane] = new_v;
+            }
         }
     }
+    // kvq_decode_step, on the split that holds the new token (the request's
+    // last split) once the request's verdict is known: KV head 0 reports
+    // it, and a request that passed gets the staged row written.
+    auto finish_here = [&](bool stale) {
+        if (kvh == 0 && threadIdx.x == 0)
+            a.abort_out[b] = stale ? 1 : 0;
+        const int64_t tpos = len - 1;
+        const int32_t page = page_list[static_cast<int>(tpos / ps) - first_page];
+        if (stale || threadIdx.x >= 32 || page < 0 || page >= a.num_pages)
+            return;
+        const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + tpos % ps;
+        const int ln = threadIdx.x;
+        *reinterpret_cast<NewRow *>(static_cast<uint8_t *>(a.k_cache) + row * T::kRowBytes + sizeof(NewRow) * ln) =
+            reinterpret_cast<const NewRow *>(new_tok)[ln];
+        *reinterpret_cast<NewRow *>(static_cast<uint8_t *>(a.v_cache) + row * T::kRowBytes + sizeof(NewRow) * ln) =
+            reinterpret_cast<const NewRow *>(new_tok + T::kRowBytes)[ln];
+    };
     auto write_new = [&]() {
         if (new_row < 0)
             return;
@@ -498,9 +527,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         write_new();
 
     if (bad) {                                             // for kvq_decode_step a failed check
-        if constexpr (kCluster)
+        if constexpr (kCluster) {
             cluster_finish(a, b, kvh, step_check ? kPartialStale : kPartialInvalid, part, finisher);
-        else
+            if (split == finisher)                         // this split failed: so did the request
+                finish_here(true);
+        } else
             drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem),
                        step_check ? kLseStale : kLseInvalid);
         return;
@@ -548,18 +579,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 
     if (step_check) {
         // kvq_decode_step: this split's share of the tag check, its own pages
-        // (whose ids are in range here), while the first copies fly.  The
-        // split attends regardless; a failure only changes what it publishes.
+        // (whose ids are in range here).  The live and expected tags come in
+        // by asynchronous copies behind the first bulk copies and are compared
+        // once the split has attended: a failure only changes what it
+        // publishes.  Thread t copies (and later compares) entries t, t + 128, ...
         const uint32_t *want = a.expected_tags + static_cast<int64_t>(b) * a.max_pages_per_seq + first_page;
-        bool stale = false;
 #pragma unroll
         for (int k = 0; k < kIdsPerThread; ++k) {
             const int i = threadIdx.x + k * kThreads;
-            if (i < n_pages)
-                stale |= __ldg(a.page_tags + page_list[i]) != __ldg(want + i);
+            if (i < n_pages) {
+                cp_async_4(tag_live + i, a.page_tags + page_list[i]);
+                cp_async_4(tag_want + i, want + i);
+            }
         }
-        if (stale)
-            s_stale = 1;
+        cp_async_commit();
     }
 
     // Query fragments (mma B operand): lane (gq, tq) holds query head gq of
@@ -812,11 +845,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         for (int j = it + 1; j < issued; ++j)
             mbar_wait_bounded(&my_full[j % T::kStages], (j / T::kStages) & 1, kWaitLimitNs);
     }
+    if (step_check) {                                      // this thread's tag entries
+        cp_async_wait_all();
+        bool stale = false;
+#pragma unroll
+        for (int k = 0; k < kIdsPerThread; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            if (i < n_pages)
+                stale |= tag_live[i] != tag_want[i];
+        }
+        if (stale)
+            s_stale = 1;
+    }
     __syncthreads();
     if (s_stale || s_failed) {                             // a failed check outranks a timeout
-        if constexpr (kCluster)
-            cluster_finish(a, b, kvh, s_stale ? kPartialStale : kPartialInvalid, part, finisher);
-        else
+        if constexpr (kCluster) {
+            const bool stale = cluster_finish(a, b, kvh, s_stale ? kPartialStale : kPartialInvalid, part, finisher);
+            if (split == finisher)
+                finish_here(stale);
+        } else
             drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem),
                        s_stale ? kLseStale : kLseInvalid);
         return;
@@ -888,11 +935,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         }
     }
     if constexpr (kCluster) {
-        cluster_finish(a, b, kvh, kPartialOk, part, finisher);
+        const bool stale = cluster_finish(a, b, kvh, kPartialOk, part, finisher);
+        if (split == finisher)
+            finish_here(stale);
     } else if (nsplit > 1) {
         publish_and_combine(a, b, kvh, nsplit, reinterpret_cast<float *>(smem) + kScratchOffset);
     } else if (step_check) {                               // one split: its own verdict
-        finish_step(a, b, kvh, false);
+        finish_here(false);
     }
 }
 

@@ -205,6 +205,24 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void *tensor_map, int32
                  : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (no register holds the value;
+// cp_async_wait_all makes it visible to the issuing thread).
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
