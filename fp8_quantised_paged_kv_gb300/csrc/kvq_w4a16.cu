@@ -53,7 +53,10 @@ constexpr int kW4ScStride = kW4MaxGroups + 2;                  // halves per col
 constexpr int kW4SmemBytes = 1024 /* alignment slack */ + kW4RingBytes + kW4Warps * kW4Stages * 8 +
                              kW4Cols * kW4ScStride * 2 /* scales */ + 16;
 constexpr uint64_t kW4WaitLimitNs = 1000000000ull;
-static_assert(16 * kW4Cols * 4 <= kW4WarpRing, "a warp's partial fits in its idle ring");
+// A warp's partial [16 rows][64 columns] in its idle ring, rows 68 floats
+// apart: the four row pairs a lane group stores land in different banks.
+constexpr int kW4RedStride = kW4Cols + 4;
+static_assert(16 * kW4RedStride * 4 <= kW4WarpRing, "a warp's partial fits in its idle ring");
 static_assert(16 * kW4Cols * 4 <= kW4Cols * kW4ScStride * 2, "the CTA's partial fits over the scales");
 
 // Byte offset of 16-byte chunk c of row `line` in a tile of 64-byte rows
@@ -292,16 +295,16 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
 
     // ---- the four warps' partials (each in its own idle ring), then the CTA's
     constexpr int kRowsT = 8 * kNT;                                  // batch rows the CTA holds
-    float *red = reinterpret_cast<float *>(ring);                    // [kRowsT][64]
+    float *red = reinterpret_cast<float *>(ring);                    // [kRowsT][kW4RedStride]
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
             const int c = mt * 16 + gq, r = nt * 8 + 2 * tq;
-            red[r * kW4Cols + c] = acc[mt][nt][0];
-            red[(r + 1) * kW4Cols + c] = acc[mt][nt][1];
-            red[r * kW4Cols + c + 8] = acc[mt][nt][2];
-            red[(r + 1) * kW4Cols + c + 8] = acc[mt][nt][3];
+            red[r * kW4RedStride + c] = acc[mt][nt][0];
+            red[(r + 1) * kW4RedStride + c] = acc[mt][nt][1];
+            red[r * kW4RedStride + c + 8] = acc[mt][nt][2];
+            red[(r + 1) * kW4RedStride + c + 8] = acc[mt][nt][3];
         }
     __syncthreads();
     float *cta = reinterpret_cast<float *>(sc_sm);                   // [kRowsT][64], scales are done
@@ -309,7 +312,7 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kW4Warps; ++w)
-            v += reinterpret_cast<const float *>(smem + w * kW4WarpRing)[o];
+            v += reinterpret_cast<const float *>(smem + w * kW4WarpRing)[(o / kW4Cols) * kW4RedStride + o % kW4Cols];
         if (s_failed)                               // a copy timed out: this tile gives zeros
             v = 0.f;
         if constexpr (kCluster) {
