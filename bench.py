@@ -39,14 +39,23 @@ W4_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w4a16_m1.json")
 W4_SOURCES = ("kvq_w4a16.cu", "kvq_ptx.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed: what a
+    kernel is built from, so that editing a comment keeps a profile valid."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(names=("kvq_decode.cu", "kvq_ptx.cuh")) -> str:
-    """Hash of the sources of a kernel (by default the decode kernel, the one
-    the decode roofline reports)."""
+    """Hash of the code (comments aside) of a kernel's sources (by default the
+    decode kernel, the one the decode roofline reports)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quantised_paged_kv_gb300", "csrc")
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -409,10 +409,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     const int64_t len = a.seq_lens[b];
     // kvq_decode_step: each split checks the tags of its own pages (together
-    // the request's used entries) while its first copies fly, and publishes
-    // a failure with its partial; the CTA that sees every split's partial
-    // (finish_step) writes the flag and, if the request passed, its new
-    // token.  A request without tokens to check is decided here.
+    // the request's used entries) while it streams them, and publishes a
+    // failure with its partial; the CTA that sees every split's partial
+    // writes the flag and, if the request passed, its new token
+    // (finish_here, or finish_step in the workspace form).  A request
+    // without tokens to check is decided here.
     const bool step_check = a.expected_tags != nullptr;
     const bool reporter = step_check && split == 0 && kvh == 0 && threadIdx.x == 0;
     const bool aborted = !step_check && a.abort_flags != nullptr && a.abort_flags[b] != 0;
@@ -423,7 +424,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int nsplit = zero_request ? 1 : static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
     float *part = reinterpret_cast<float *>(smem) + kScratchOffset;   // cluster partial
     // kvq_decode_step: the split that finishes the step of a request with
-    // tokens (the cluster's last split)
+    // tokens in the cluster form and when there is one split -- the last
+    // split, which holds the new token (the workspace form's combine
+    // finishes in whichever split arrives last)
     const int finisher = step_check && !zero_request ? nsplit - 1 : -1;
     if constexpr (kCluster) {
         if (zero_request || split >= nsplit) {             // no tokens: weight 0

@@ -141,3 +141,44 @@ def test_decode_step_argument_checks():
                              ctypes.c_float(w.softmax_scale), kvq._ptr(dw.k_new), kvq._ptr(dw.v_new),
                              kvq._ptr(out), 0, kvq._ptr(ws), ws_bytes, 0, None)
     assert st == 1                                       # no expected tags: invalid argument
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_decode_step_consecutive_steps(splits):
+    """Four steps in a row, each appending one more token that the next step
+    reads back from the cache; a page handed to another owner between steps
+    (its live tag bumped) aborts its request from then on.  Flags, caches and
+    outputs equal the separate calls after every step."""
+    steps = 4
+    final = np.array([40, 129, 300, 17, 1000, 64], np.int64)
+    w = W.make_custom(final, group=4, page_size=16, seed=90 + splits)
+    w.seq_lens = (final - (steps - 1)).astype(np.int32)          # the prefill ends steps - 1 earlier
+    sep = DeviceWorkload(w, kvq.KVQ_CACHE_FP8_E4M3)
+    one = DeviceWorkload(w, kvq.KVQ_CACHE_FP8_E4M3)
+    assert torch.equal(sep.k_cache, one.k_cache)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(5)
+    for s in range(steps):
+        if s:
+            for dw in (sep, one):
+                dw.seq_lens += 1
+        if s == 2:                                                # request 4's page 10 is reallocated
+            page = int(w.block_table[4, 10])
+            for dw in (sep, one):
+                dw.page_tags[page] += 1
+        kn = W.normal_bf16_torch(tuple(sep.k_new.shape), gen, DEV, 0.0)
+        vn = W.normal_bf16_torch(tuple(sep.v_new.shape), gen, DEV, 0.0)
+        for dw in (sep, one):
+            dw.k_new.copy_(kn)
+            dw.v_new.copy_(vn)
+        out_s, out_o = sep.out(False), one.out(False)
+        sep.tag_check()
+        kvq.kvq_decode_attn_append(sep.desc, sep.q, sep.k_cache, sep.v_cache, sep.k_scale, sep.v_scale,
+                                   sep.block_table, sep.seq_lens, w.softmax_scale, sep.abort, sep.k_new,
+                                   sep.v_new, out_s, sep.workspace(splits), splits)
+        one.abort.fill_(0xCC)
+        one.decode_step(out_o, one.workspace(splits), splits)
+        torch.cuda.synchronize()
+        _assert_same(sep, one, out_s, out_o, False)
+        assert int(one.abort[4]) == (1 if s >= 2 else 0)
+        assert int(one.abort.sum()) == (1 if s >= 2 else 0)
