@@ -87,7 +87,7 @@ def dist_info():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples (every 200 ms), each stamped with the
+    """nvidia-smi clock / throttle samples (every 100 ms), each stamped with the
     host time it arrived, so the ones inside the timed region can be picked."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -105,7 +105,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
