@@ -194,8 +194,10 @@ KVQ_API kvq_status kvq_quantize_pages(const kvq_cache_desc *src_desc, const void
                                       kvq_stream_t stream);
 
 /*
- * kvq_decode_plan -- HOST-only query: how kvq_decode_attn will split the
- * context and how many workspace bytes it needs.
+ * kvq_decode_plan -- HOST-only query: how kvq_decode_attn (and the calls
+ * that run the same kernel: kvq_decode_attn_append, kvq_decode_step,
+ * kvq_decode_attn_static_ws) will split the context and how many workspace
+ * bytes it needs.
  *
  *   num_splits     requested splits per (request, KV head); 0 = automatic
  *                  (sized from the device's SM count and the batch).  A split
