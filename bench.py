@@ -224,6 +224,8 @@ def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
         return 0
+    import workloads as W
+    full = W.make(args.workload, seed=0)               # the workload the GPU arm times
     run, kv_bytes, cores, w = cpu_oracle_step_runner(args.workload, requests=1)
     for _ in range(args.warmup):
         run()
@@ -239,10 +241,12 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "sampled_requests": w.batch,
-                   "kv_tokens_per_step": w.kv_tokens(),
+        "config": {"workload": args.workload, "batch": full.batch, "kv_tokens": full.kv_tokens(),
                    "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
-                   "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3"},
+                   "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3",
+                   "out": "bf16", "step": "tag check, append and attention of each sampled request",
+                   "sampled_requests": w.batch, "kv_tokens_per_step": w.kv_tokens(),
+                   "parallelism": "host cores of rank 0"},
         "tokens_per_s": round(w.batch / (ms / 1e3), 3),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
