@@ -70,6 +70,7 @@ _SIGS = {
     "kvq_decode_step": ["desc", "p", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "p", "p", "p",
                         "f32", "p", "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_w4a16_plan": ["i32", "i32", "i32", "i32", "p"],
+    "kvq_read_probe": ["p", "size", "p", "p"],
     "kvq_w4a16_gemm": ["p", "p", "p", "i32", "i32", "i32", "p", "i32", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
     "kvq_amax_scales": ["desc", "p", "p", "p", "i32", "p", "p", "p"],
@@ -321,6 +322,16 @@ def kvq_decode_step(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, se
         out_dtype, _ptr(workspace), ws_bytes, num_splits, _stream(stream))
     _check("kvq_decode_step", st)
     return out
+
+
+def kvq_read_probe(src, sink, stream=None):
+    """Calibration: read every byte of the CUDA tensor ``src`` once with a
+    plain streaming kernel, XOR-ing its 32-bit words into ``sink`` (a
+    zeroed 1-element int32/uint32 CUDA tensor)."""
+    nbytes = src.numel() * src.element_size()
+    if sink.element_size() != 4 or sink.numel() < 1:
+        raise ValueError("sink: expected a 32-bit CUDA tensor")
+    _check("kvq_read_probe", load().kvq_read_probe(_ptr(src), nbytes, _ptr(sink), _stream(stream)))
 
 
 def kvq_w4a16_plan(m: int, n: int, k: int, num_splits: int = 0) -> int:

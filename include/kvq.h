@@ -357,6 +357,17 @@ KVQ_API kvq_status kvq_w4a16_gemm(const void *x, const uint8_t *w, const void *s
                                   kvq_stream_t stream);
 
 /*
+ * kvq_read_probe -- calibration, not part of the decode path: read `bytes`
+ * of device memory at `src` once, with a plain streaming kernel (16-byte
+ * loads, a grid of 8 CTAs x 256 threads per SM), and XOR every 32-bit word
+ * into *sink (device, uint32; the caller zeroes it first).  Timed like the
+ * decode kernels, it says how fast one launch reads that many bytes on this
+ * GPU.  src and bytes must be multiples of 16 (KVQ_ERR_INVALID_ARG
+ * otherwise); bytes == 0 does nothing.
+ */
+KVQ_API kvq_status kvq_read_probe(const void *src, size_t bytes, uint32_t *sink, kvq_stream_t stream);
+
+/*
  * kvq_decode_attn_static_ws -- kvq_decode_attn for callers that cannot
  * allocate device memory while they decode (an engine that has already
  * handed all of its device memory to its own pool, or C code that holds no

@@ -394,3 +394,17 @@ def test_decode_attn_append_edge_requests():
         for r in (1, 2, 3, 4):
             assert np.all(got[r] == 0.0), (splits, r)
         assert torch.equal(out_f.view(torch.int32), out_s.view(torch.int32))
+
+
+def test_read_probe_reads_every_word_once():
+    """The calibration probe XORs every 32-bit word: compare with numpy, for a
+    size that leaves a ragged tail of the grid-stride loop."""
+    rng = np.random.default_rng(3)
+    for n_words in (4, 4 * 1000 + 8, (1 << 22) + 36):
+        host = rng.integers(0, 2**32, size=n_words, dtype=np.uint64).astype(np.uint32)
+        src = torch.from_numpy(host.view(np.int32)).to(DEV)
+        sink = torch.zeros(1, dtype=torch.int32, device=DEV)
+        kvq.kvq_read_probe(src, sink)
+        torch.cuda.synchronize()
+        want = np.bitwise_xor.reduce(host)
+        assert int(sink.cpu().numpy().view(np.uint32)[0]) == int(want), n_words
