@@ -359,8 +359,8 @@ KVQ_API kvq_status kvq_w4a16_gemm(const void *x, const uint8_t *w, const void *s
 /*
  * kvq_read_probe -- calibration, not part of the decode path: read `bytes`
  * of device memory at `src` once, with a plain streaming kernel (16-byte
- * loads, a grid of 8 CTAs x 256 threads per SM), and XOR every 32-bit word
- * into *sink (device, uint32; the caller zeroes it first).  Timed like the
+ * loads, 8 CTAs x 256 threads per SM, each CTA one contiguous slice), and
+ * XOR every 32-bit word into *sink (device, uint32; the caller zeroes it first).  Timed like the
  * decode kernels, it says how fast one launch reads that many bytes on this
  * GPU.  src and bytes must be multiples of 16 (KVQ_ERR_INVALID_ARG
  * otherwise); bytes == 0 does nothing.
