@@ -67,9 +67,16 @@ struct Plan {
 // splits).
 int64_t auto_splits(int64_t pairs, int64_t max_ctx, int64_t slots)
 {
+    // Long jobs: splits of up to 8,192 tokens.  The plan knows only the
+    // longest context; when that gives between 4 and 8 waves, requests
+    // shorter than it (a mixed batch) leave the last waves ragged, and
+    // splits half as long fill them better (ragged64: 359 us against 372 us;
+    // long4, at 8 waves and more, is 5 % slower with the shorter splits).
     const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
-    if (pairs * big >= 4 * slots)
+    if (pairs * big >= 8 * slots)
         return big;
+    if (pairs * big >= 4 * slots)
+        return 2 * big;
     int64_t most = max_ctx / kMinAutoSplitTokens;
     if (most < 1)
         most = 1;

@@ -160,15 +160,17 @@ __device__ void finish_step(const DecodeArgs &a, int b, int kvh, bool stale)
 __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsplit, float *scratch)
 {
     __shared__ int s_last;
-    __threadfence();                         // this split's partial is visible before it is counted
+    // The block barrier orders every thread's partial before thread 0's
+    // release; the last split's acquire, then its barrier, orders all the
+    // peers' partials before its loads (the counter is the only
+    // synchronisation between the splits).
     __syncthreads();
     unsigned int *counter = a.counters + static_cast<int64_t>(b) * a.num_kv_heads + kvh;
     if (threadIdx.x == 0)
-        s_last = atomicAdd(counter, 1u) == static_cast<unsigned int>(nsplit - 1);
+        s_last = atom_add_acq_rel_gpu(counter, 1u) == static_cast<unsigned int>(nsplit - 1);
     __syncthreads();
     if (!s_last)
         return;
-    __threadfence();
     const int g = a.group, n = nsplit;
     const int64_t bh0 = static_cast<int64_t>(b) * a.num_q_heads + kvh * g;
     float *s_tot = scratch;                  // [8] sum of weights (0: drop the head)

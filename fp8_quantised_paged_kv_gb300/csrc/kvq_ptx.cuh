@@ -205,6 +205,15 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void *tensor_map, int32
                  : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old
+// value.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int *p, unsigned int v)
+{
+    unsigned int old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // 4-byte asynchronous copy global -> shared (no register holds the value;
 // cp_async_wait_all makes it visible to the issuing thread).
 __device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src)
