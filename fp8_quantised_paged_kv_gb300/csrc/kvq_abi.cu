@@ -99,6 +99,56 @@ int64_t auto_splits(int64_t pairs, int64_t max_ctx, int64_t slots)
     return best;
 }
 
+// Split count for a job that can run in one wave, or 0 if none can.  Among
+// the counts whose CTAs are all resident at once -- every (request, KV
+// head) as one resident cluster of its splits, or as plain CTAs -- it takes
+// the smallest estimate of
+//   fixed cost + smooth max(all bytes / HBM rate, one split's bytes / the
+//   rate one CTA's copy pipeline sustains) + the combine's tail,
+// the constants measured on GB300: a CTA streams about 20 GB/s (FP8; 40 for
+// the BF16 tile, whose copies are twice as large), the combine costs about
+// 2.5 us through distributed shared memory and 9 us through the workspace.
+// (16 requests x 8,193 tokens: 3 splits in clusters, 58.5 us, where the
+// multi-wave rule took 7 through the workspace, 79.6 us; 32 x 4,097: one
+// split, 62.0 us against 73.5 us.)
+int64_t single_wave_splits(int64_t pairs, int64_t max_ctx, int64_t unit, int64_t slots, bool bf16)
+{
+    const double bytes_per_tok = bf16 ? 512.0 : 256.0;       // K + V of one token of one KV head
+    const double cta_rate = bf16 ? 40e9 : 20e9;               // bytes per second per CTA
+    const double hbm_rate = 6.3e12;
+    const double total_us = static_cast<double>(pairs) * static_cast<double>(max_ctx) * bytes_per_tok / hbm_rate * 1e6;
+    int64_t most = max_ctx / kMinAutoSplitTokens;
+    if (most < 1)
+        most = 1;
+    if (most > kvq::kMaxSplitsTotal)
+        most = kvq::kMaxSplitsTotal;
+    int64_t best = 0, last = 0;
+    double best_us = 1e30;
+    for (int64_t n = 1; n <= most; ++n) {
+        int64_t split = (max_ctx + n - 1) / n;
+        split = (split + unit - 1) / unit * unit;
+        if (split > kMaxSplitTokens)
+            continue;
+        const int64_t splits = (max_ctx + split - 1) / split;
+        if (splits == last)
+            continue;                                           // the same plan as a smaller n
+        last = splits;
+        const bool cluster = splits >= 2 && splits <= kvq::kMaxCluster &&
+                             pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16);
+        if (!cluster && pairs * splits > slots)
+            continue;                                           // more than one wave
+        const double split_us = static_cast<double>(split) * bytes_per_tok / cta_rate * 1e6;
+        const double stream_us = std::pow(std::pow(total_us, 4.0) + std::pow(split_us, 4.0), 0.25);
+        const double combine_us = splits == 1 ? 0.0 : cluster ? 2.5 : 9.0;
+        const double est = 11.0 + stream_us + combine_us;
+        if (est < best_us - 1e-9) {
+            best_us = est;
+            best = splits;
+        }
+    }
+    return best;
+}
+
 kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads,
                      int32_t max_pages, int32_t num_splits, Plan *p)
 {
@@ -116,19 +166,24 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         return KVQ_ERR_UNSUPPORTED;
     const int64_t max_ctx = static_cast<int64_t>(max_pages) * d->page_size;
     const int64_t unit = d->page_size > kChunkTokens ? d->page_size : kChunkTokens;
+    const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
+    const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads;
     int64_t want;
+    bool single_wave = false;
     if (num_splits > 0) {
         want = num_splits;
     } else {
-        const int64_t slots = static_cast<int64_t>(sm_count()) *
-                              kvq::decode_ctas_per_sm(d->cache_dtype == KVQ_CACHE_BF16);
-        want = auto_splits(static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads, max_ctx, slots);
+        const int64_t slots = static_cast<int64_t>(sm_count()) * kvq::decode_ctas_per_sm(bf16);
+        const int64_t jobs = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads;
+        const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
+        want = jobs * big < 4 * slots ? single_wave_splits(jobs, max_ctx, unit, slots, bf16) : 0;
+        single_wave = want > 0;
+        if (!single_wave)
+            want = auto_splits(jobs, max_ctx, slots);
     }
     if (want < 1)
         want = 1;
-    const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
-    const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads;
-    if (num_splits == 0 && want >= 2 && batch > 0) {
+    if (num_splits == 0 && !single_wave && want >= 2 && batch > 0) {
         // A job whose splits could all be resident as clusters merges them
         // through distributed shared memory, a much shorter tail than the
         // workspace combine; that is worth giving up up to half the splits.
