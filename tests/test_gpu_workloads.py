@@ -122,3 +122,20 @@ def test_packed_step_inputs_give_the_same_step():
     dw.step(out2, dw.workspace(0))
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+@pytest.mark.parametrize("lens,group", [([8193] * 16, 8), ([4097] * 32, 4), ([2049] * 64, 4)])
+def test_mid_size_plans_sampled(lens, group):
+    """Mid-size batches (268 MB each) with the plans the planner picks for them
+    (a one-wave cluster of 3 splits, one split, a multi-wave workspace plan),
+    through the one-launch step; sampled requests against the oracle."""
+    w = W.make_custom(lens, group=group, page_size=16, num_kv_heads=8, seed=3, pool_factor=1.2)
+    dw = DeviceWorkload(w, FP8)
+    out = dw.out(False)
+    print("plan", kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads, w.max_pages_per_seq, 0))
+    dw.abort.fill_(1)
+    dw.decode_step(out, dw.workspace(0))
+    torch.cuda.synchronize()
+    assert int(dw.abort.sum().item()) == 0
+    for r in (0, len(lens) // 2, len(lens) - 1):
+        _check_request(dw, out, r, "bf16")
