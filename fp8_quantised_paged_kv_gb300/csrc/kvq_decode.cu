@@ -304,17 +304,23 @@ __device__ bool cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
                      kLseStale;
         s_any_stale = stale;
     }
-    for (int h = rank; h < g; h += n)
-    for (int d = threadIdx.x; d < kHeadDim; d += kThreads) {
-        float lse[kMaxCluster], ov[kMaxCluster];
+    // thread t takes dims 4 (t % 32) .. + 3 of head h0 + t / 32 (16-byte
+    // loads from each peer), 4 of this CTA's heads per pass
+    for (int h0 = rank; h0 < g; h0 += kThreads / 32 * n) {
+        const int h = h0 + (threadIdx.x / 32) * n;
+        if (h >= g)
+            continue;
+        const int d = 4 * (threadIdx.x % 32);
+        float lse[kMaxCluster];
+        float4 ov[kMaxCluster];
 #pragma unroll
         for (int s = 0; s < kMaxCluster; ++s) {
             lse[s] = -INFINITY;
-            ov[s] = 0.f;
+            ov[s] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (s < n) {
                 const uint32_t peer = map_shared_rank(base, static_cast<uint32_t>(s));
                 lse[s] = ld_shared_cluster_f32(peer + 4u * h);
-                ov[s] = ld_shared_cluster_f32(peer + 4u * (kMaxGroup + h * kHeadDim + d));
+                ov[s] = ld_shared_cluster_v4(peer + 4u * (kMaxGroup + h * kHeadDim + d));
             }
         }
         float m = -INFINITY;
@@ -324,17 +330,25 @@ __device__ bool cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
             bad |= lse[s] != lse[s];
             m = fmaxf(m, lse[s]);
         }
-        float sum = 0.f, acc = 0.f;
+        float sum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int s = 0; s < kMaxCluster; ++s) {
             if (lse[s] != -INFINITY) {
                 const float w = fast_exp2(lse[s] - m);
                 sum += w;
-                acc += w * ov[s];
+                acc.x += w * ov[s].x;
+                acc.y += w * ov[s].y;
+                acc.z += w * ov[s].z;
+                acc.w += w * ov[s].w;
             }
         }
-        store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * kHeadDim + d,
-                  (bad || !(sum > 0.f)) ? 0.f : acc / sum, a.out_fp32);
+        const bool zero = bad || !(sum > 0.f);
+        const int64_t o0 = (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * kHeadDim + d;
+        store_out(a.out, o0, zero ? 0.f : acc.x / sum, a.out_fp32);
+        store_out(a.out, o0 + 1, zero ? 0.f : acc.y / sum, a.out_fp32);
+        store_out(a.out, o0 + 2, zero ? 0.f : acc.z / sum, a.out_fp32);
+        store_out(a.out, o0 + 3, zero ? 0.f : acc.w / sum, a.out_fp32);
     }
     cluster_sync();                          // also orders s_any_stale within the CTA
     return rank == finisher && s_any_stale != 0;
