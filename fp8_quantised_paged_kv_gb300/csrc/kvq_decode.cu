@@ -203,36 +203,45 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
             s_tot[h] = bad ? 0.f : sum;
     }
     __syncthreads();
-    // thread d: every head of the group, all splits, loads independent across heads
-    for (int d = threadIdx.x; d < kHeadDim; d += kThreads) {
-        float acc[kMaxGroup];
+    // thread t: the (head, 4 dims) pairs t and t + 128 of the group's 8 x 32;
+    // eight splits per round, every 16-byte load of a round issued before any
+    // is used, so a round costs one trip to L2
+    constexpr int kRound = 8;
+    static_assert(kMaxGroup * (kHeadDim / 4) == 2 * kThreads, "two (head, 4 dims) pairs per thread");
+    const int hp[2] = {static_cast<int>(threadIdx.x) / 32, static_cast<int>(threadIdx.x + kThreads) / 32};
+    const int cp = 4 * (threadIdx.x % 32);
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int s0 = 0; s0 < n; s0 += kRound) {
+        float4 v[2][kRound];
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h)
-            acc[h] = 0.f;
-        // four splits per round: all of the round's loads are issued before
-        // any is used, so a round costs one trip to L2
-        for (int s0 = 0; s0 < n; s0 += 4) {
-            float v[4][kMaxGroup];
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < kRound; ++j)
+                v[q][j] = (hp[q] < g && s0 + j < n)
+                              ? __ldcg(reinterpret_cast<const float4 *>(
+                                    a.ws_o + ((bh0 + hp[q]) * a.max_splits + s0 + j) * kHeadDim + cp))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int h = 0; h < kMaxGroup; ++h)
-                    v[j][h] = (h < g && s0 + j < n)
-                                  ? __ldcg(a.ws_o + ((bh0 + h) * a.max_splits + s0 + j) * kHeadDim + d)
-                                  : 0.f;
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int h = 0; h < kMaxGroup; ++h)
-                    if (h < g && s0 + j < n)
-                        acc[h] += s_w[h * n + s0 + j] * v[j][h];
-        }
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h)
-            if (h < g)
-                store_out(a.out, (bh0 + h) * kHeadDim + d, s_tot[h] > 0.f ? acc[h] / s_tot[h] : 0.f,
-                          a.out_fp32);
+            for (int j = 0; j < kRound; ++j)
+                if (hp[q] < g && s0 + j < n) {
+                    const float wt = s_w[hp[q] * n + s0 + j];
+                    acc[q].x += wt * v[q][j].x;
+                    acc[q].y += wt * v[q][j].y;
+                    acc[q].z += wt * v[q][j].z;
+                    acc[q].w += wt * v[q][j].w;
+                }
     }
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        if (hp[q] < g) {
+            const int64_t o0 = (bh0 + hp[q]) * kHeadDim + cp;
+            store_out(a.out, o0, s_tot[hp[q]] > 0.f ? acc[q].x / s_tot[hp[q]] : 0.f, a.out_fp32);
+            store_out(a.out, o0 + 1, s_tot[hp[q]] > 0.f ? acc[q].y / s_tot[hp[q]] : 0.f, a.out_fp32);
+            store_out(a.out, o0 + 2, s_tot[hp[q]] > 0.f ? acc[q].z / s_tot[hp[q]] : 0.f, a.out_fp32);
+            store_out(a.out, o0 + 3, s_tot[hp[q]] > 0.f ? acc[q].w / s_tot[hp[q]] : 0.f, a.out_fp32);
+        }
     if (a.expected_tags != nullptr) {        // kvq_decode_step: the request's verdict
         __shared__ int s_stale_any;
         if (threadIdx.x == 0) {
