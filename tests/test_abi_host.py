@@ -162,3 +162,17 @@ def test_w4a16_plan_and_argument_checks():
     assert st == 1                                        # null pointers: invalid argument
     st = lib.kvq_w4a16_gemm(None, None, None, 0, 64, 256, None, 0, 0, None)
     assert st == 0                                        # empty batch: nothing to do
+
+
+@pytest.mark.parametrize("B,hq,ps,maxp,want", [
+    (8, 64, 16, 513, (1376, 6)),       # uniform8: six splits fill one wave
+    (64, 32, 64, 511, (4096, 8)),      # ragged64: 4-8 waves at the longest context -> halved splits
+    (4, 16, 64, 16384, (8192, 128)),   # long4: >= 8 waves -> 8,192-token splits
+    (32, 32, 16, 257, (4128, 1)),      # 32 x 4,097: one split beats a workspace combine
+    (64, 32, 16, 129, (1056, 2)),      # 64 x 2,049: no one-wave plan -> wave-filling rule
+])
+def test_planner_choices_on_a_host_without_a_gpu(B, hq, ps, maxp, want):
+    """The planner's automatic choices with the host fallback (148 SMs, no
+    clusters): the wave rules for long jobs and the one-wave estimate."""
+    st, ms, _ = _plan(ps=ps, hkv=8, B=B, hq=hq, maxp=maxp)
+    assert (st, ms) == want
