@@ -14,6 +14,9 @@
 // quantise pass reads 2 B and writes 1 B per element.  Both run one wave of
 // 256-thread CTAs (8 per SM for amax, 4 for quantise); a warp streams one
 // (page, head) tile at a time with eight 16-byte loads in flight per lane.
+// Each quotient is the correctly rounded one, as the append rule's IEEE
+// division gives it, but from a multiplication by RN(1 / scale) and one
+// correction step (quotient_rn): no division per element.
 // The tile loads are streaming loads (evict first): they do not push out
 // of L2 what is already there (dirty lines that would have to be written
 // back meanwhile), which made the amax pass 13 % faster.
@@ -112,6 +115,35 @@ __global__ void scales_kernel(HandoffArgs a)
     }
 }
 
+// One warp's (page, head) tile: per_tile 16-byte bf16 vectors to 8-byte
+// e4m3 vectors, eight loads in flight per lane.  kRcp: the quotients from
+// quotient_rn; otherwise one IEEE division each (scales outside its range).
+template <bool kRcp>
+__device__ __forceinline__ void quantize_tile(const uint4 *__restrict__ src, uint2 *__restrict__ dst,
+                                              int per_tile, int lane, const QuotientRcp &c)
+{
+    for (int e0 = 0; e0 < per_tile; e0 += 32 * kVecsPerLane) {
+        uint4 x[kVecsPerLane];
+#pragma unroll
+        for (int k = 0; k < kVecsPerLane; ++k) {
+            const int e = e0 + k * 32 + lane;
+            x[k] = e < per_tile ? __ldcs(src + e) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kVecsPerLane; ++k) {
+            const int e = e0 + k * 32 + lane;
+            if (e < per_tile) {
+                if constexpr (kRcp)
+                    dst[e] = make_uint2(encode4_e4m3_rcp(x[k].x, x[k].y, c),
+                                        encode4_e4m3_rcp(x[k].z, x[k].w, c));
+                else
+                    dst[e] = make_uint2(encode4_e4m3(x[k].x, x[k].y, c.scale),
+                                        encode4_e4m3(x[k].z, x[k].w, c.scale));
+            }
+        }
+    }
+}
+
 // One warp per (listed pair, K|V, KV head) tile at a time, grid-stride over
 // the tiles; eight 16-byte loads (64 bf16 elements) in flight per lane; the
 // next tile's page ids are loaded while the current one streams.  Every
@@ -139,21 +171,11 @@ __global__ void __launch_bounds__(kHandoffThreads, kCtasPerSmQuant) quantize_pag
             uint2 *dst = reinterpret_cast<uint2 *>(kv ? a.v_dst : a.k_dst) +
                          (static_cast<int64_t>(cur.y) * a.num_kv_heads + h) * per_tile;
             const float scale = __ldg((kv ? a.v_scale : a.k_scale) + h);
-            for (int e0 = 0; e0 < per_tile; e0 += 32 * kVecsPerLane) {
-                uint4 x[kVecsPerLane];
-#pragma unroll
-                for (int k = 0; k < kVecsPerLane; ++k) {
-                    const int e = e0 + k * 32 + lane;
-                    x[k] = e < per_tile ? __ldcs(src + e) : make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int k = 0; k < kVecsPerLane; ++k) {
-                    const int e = e0 + k * 32 + lane;
-                    if (e < per_tile)
-                        dst[e] = make_uint2(encode4_e4m3(x[k].x, x[k].y, scale),
-                                            encode4_e4m3(x[k].z, x[k].w, scale));
-                }
-            }
+            QuotientRcp c;
+            if (quotient_rcp_init(scale, c))
+                quantize_tile<true>(src, dst, per_tile, lane, c);
+            else
+                quantize_tile<false>(src, dst, per_tile, lane, c);
         }
         cur = next;
     }

@@ -68,6 +68,49 @@ __device__ __forceinline__ uint32_t encode4_e4m3(uint32_t w0, uint32_t w1, float
     return static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
 }
 
+// The correctly rounded fp32 quotient x / scale without a division, for
+// scales in [2^-90, 2^100]: with rcp = RN(1 / scale), q0 = RN(x * rcp) and the
+// exact remainder r = scale * q0 - x (one fma), RN(q0 - r * rcp) is RN(x / scale)
+// (Markstein's correction step; checked exhaustively over every bf16
+// significand of x against every fp32 significand of the scale).  x is first
+// clamped to +-1024 * scale, NaN kept: a clamped quotient is +-1024, which
+// saturates like the true one, and no intermediate overflows.  Within the
+// scale range every intermediate that decides an e4m3 code (|x / scale| >=
+// 2^-12) is normal or exact, and the remainder's sign rule keeps -0 as -0.
+struct QuotientRcp {
+    float scale, rcp, lim;
+};
+
+// The per-scale constants; ok is false outside the range above (then the
+// caller divides).
+__device__ __forceinline__ bool quotient_rcp_init(float scale, QuotientRcp &c)
+{
+    c.scale = scale;
+    c.rcp = __frcp_rn(scale);
+    c.lim = 1024.0f * scale;
+    return scale >= 0x1p-90f && scale <= 0x1p100f;
+}
+
+__device__ __forceinline__ float quotient_rn(float x, const QuotientRcp &c)
+{
+    float xc;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(xc) : "f"(x), "f"(c.lim));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(xc) : "f"(xc), "f"(-c.lim));
+    const float q0 = __fmul_rn(xc, c.rcp);
+    const float r = __fmaf_rn(c.scale, q0, -xc);
+    return __fmaf_rn(r, -c.rcp, q0);
+}
+
+// encode4_e4m3 with the quotients from quotient_rn (the same codes).
+__device__ __forceinline__ uint32_t encode4_e4m3_rcp(uint32_t w0, uint32_t w1, const QuotientRcp &c)
+{
+    const float2 p0 = bf16x2_to_f32x2(w0);
+    const float2 p1 = bf16x2_to_f32x2(w1);
+    const uint16_t c01 = f32x2_to_e4m3x2(quotient_rn(p0.x, c), quotient_rn(p0.y, c));
+    const uint16_t c23 = f32x2_to_e4m3x2(quotient_rn(p1.x, c), quotient_rn(p1.y, c));
+    return static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+}
+
 // Eight consecutive elements of one K or V row: bf16 x (16 bytes) becomes
 // eight e4m3 codes e4m3(x / scale) -- one IEEE fp32 division each, rounding
 // to nearest even, saturating at +-448 -- stored as 8 bytes at dst; or, for

@@ -50,6 +50,46 @@ def test_amax_scales_and_quantize_pages_bit_exact(ps):
     assert np.array_equal(to_np_bits(kd), kref) and np.array_equal(to_np_bits(vd), vref)
 
 
+def _split_nan(values_f32, codes_gpu, codes_ref):
+    """NaN inputs may map to either NaN code; everything else must match bit for bit."""
+    nan = np.isnan(values_f32)
+    assert np.array_equal(codes_gpu[~nan], codes_ref[~nan])
+    assert np.all((codes_gpu[nan] & 0x7F) == 0x7F)
+
+
+@pytest.mark.parametrize("scales", [
+    [1.0, 0.37, 3.1e-3, 17.5, 1e-30, 1e30, 2.0 ** -20, 3e38],
+    [0.011, 0.0123, 0.2, 0.75, 1.0 / 448.0, 5.0 / 448.0, 100.0 / 448.0, 7.77],
+])
+def test_quantize_pages_every_bf16_value_bit_exact(scales):
+    """Every bf16 bit pattern in every head, under given scales: the same codes
+    as one IEEE division per element (scale 1 puts inputs on e4m3 ties; 3e38 has
+    a subnormal reciprocal; 1e-30 overflows the quotient)."""
+    ps, H, N = 16, 8, 32
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(N, 1, ps, 128)
+    kbits = np.ascontiguousarray(np.broadcast_to(bits, (N, H, ps, 128)))
+    vbits = kbits ^ np.uint16(0x8000)
+    ksrc = torch.from_numpy(kbits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    vsrc = torch.from_numpy(vbits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    sk = np.array(scales, np.float32)
+    sv = sk[::-1].copy()
+    src = np.arange(N, dtype=np.int32)
+    dst = np.random.default_rng(5).permutation(N).astype(np.int32)
+    src_desc = kvq.CacheDesc(N, ps, H, 128, kvq.KVQ_CACHE_BF16)
+    dst_desc = kvq.CacheDesc(N, ps, H, 128, kvq.KVQ_CACHE_FP8_E4M3)
+    kd = torch.full((N, H, ps, 128), 0xA5, dtype=torch.uint8, device=DEV)
+    vd = kd.clone()
+    kvq.kvq_quantize_pages(src_desc, ksrc, vsrc, torch.from_numpy(src).to(DEV), dst_desc, kd, vd,
+                           torch.from_numpy(dst).to(DEV), torch.from_numpy(sk).to(DEV),
+                           torch.from_numpy(sv).to(DEV))
+    kref = np.zeros((N, H, ps, 128), np.uint8)
+    vref = np.zeros_like(kref)
+    oracle.quantize_pages(kbits, vbits, src, kref, vref, dst, sk, sv)
+    for ref, got, b, sc in ((kref, to_np_bits(kd), kbits, sk), (vref, to_np_bits(vd), vbits, sv)):
+        vals = W.bf16_bits_to_f32(b[src]) / sc[None, :, None, None]
+        _split_nan(vals, got[dst], ref[dst])
+
+
 def test_decode_over_handed_over_pages():
     """A request prefilled in a bf16 cache, handed to an e4m3 cache, then decoded."""
     ps, H, g, L = 16, 8, 8, 1500
