@@ -69,20 +69,22 @@ __device__ __forceinline__ uint32_t encode4_e4m3(uint32_t w0, uint32_t w1, float
 }
 
 // The correctly rounded fp32 quotient x / scale without a division, for
-// scales in [2^-90, 2^100]: with rcp = RN(1 / scale), q0 = RN(x * rcp) and the
-// exact remainder r = scale * q0 - x (one fma), RN(q0 - r * rcp) is RN(x / scale)
-// (Markstein's correction step; checked exhaustively over every bf16
-// significand of x against every fp32 significand of the scale).  x is first
-// clamped to +-1024 * scale, NaN kept: a clamped quotient is +-1024, which
-// saturates like the true one, and no intermediate overflows.  Within the
-// scale range every intermediate that decides an e4m3 code (|x / scale| >=
-// 2^-12) is normal or exact, and the remainder's sign rule keeps -0 as -0.
+// scales in [2^-90, 2^100].  With rcp = RN(1 / scale), q0 = RN(x * rcp) and
+// the exact remainder r = scale * q0 - x (one fma), RN(q0 - r * rcp) is
+// RN(x / scale): the correction step of P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990, checked here exhaustively over every bf16 significand of
+// x against every fp32 significand of the scale.  x is first clamped to
+// +-1024 * scale, NaN kept: a clamped quotient is +-1024, which saturates like
+// the true one, and no intermediate overflows.  Within the scale range every
+// intermediate that decides an e4m3 code (|x / scale| >= 2^-12) is normal or
+// exact, and the remainder's sign rule keeps -0 as -0.
 struct QuotientRcp {
     float scale, rcp, lim;
 };
 
-// The per-scale constants; ok is false outside the range above (then the
-// caller divides).
+// The per-scale constants; false outside the scale range above, where the
+// caller divides instead.
 __device__ __forceinline__ bool quotient_rcp_init(float scale, QuotientRcp &c)
 {
     c.scale = scale;
