@@ -181,8 +181,11 @@ KVQ_API kvq_status kvq_amax_scales(const kvq_cache_desc *desc, const void *k_cac
 /*
  * kvq_quantize_pages -- bf16 page src_pages[i] of (k_src, v_src) becomes
  * e4m3 page dst_pages[i] of (k_dst, v_dst): every element e4m3(x / scale[h])
- * by the kvq_append rule (fp32 division, round to nearest even, saturate at
- * +-448).  src_desc must be a bf16 cache and dst_desc an e4m3 cache with the
+ * by the kvq_append rule (the correctly rounded fp32 quotient, round to
+ * nearest even, saturate at +-448), so the codes equal kvq_append's bit for
+ * bit.  For scales in [2^-90, 2^100] the kernel reaches that quotient without
+ * a division (reciprocal, then one fused multiply-add correction); other
+ * scales divide.  src_desc must be a bf16 cache and dst_desc an e4m3 cache with the
  * same page size and KV-head count.  A pair with an out-of-range source or
  * destination id is skipped; destination pages listed twice race.
  */
