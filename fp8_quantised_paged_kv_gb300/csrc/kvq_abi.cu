@@ -1,11 +1,36 @@
 // kvq_abi.cu -- the extern "C" boundary declared in include/kvq.h: host-side
 // argument checks, split planning, tensor-map encoding and kernel launches.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/kvq.h"
 #include "kvq_internal.h"
+
+namespace kvq {
+
+int device_sm_count()
+{
+    constexpr int kHostFallbackSms = 152;
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return kHostFallbackSms;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0)
+            return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = kHostFallbackSms;
+    if (dev >= 0 && dev < 64)
+        cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+} // namespace kvq
 
 namespace {
 
@@ -16,22 +41,6 @@ constexpr int kMaxSplitTokens = 8192;
 constexpr int kMinAutoSplitTokens = 128;   // one 32-token chunk per warp
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int sm_count()
-{
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 148;
-    if (dev < 64 && cache[dev] > 0)
-        return cache[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        n = 148;
-    if (dev < 64)
-        cache[dev] = n;
-    return n;
-}
 
 kvq_status check_desc(const kvq_cache_desc *d)
 {
@@ -173,7 +182,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (num_splits > 0) {
         want = num_splits;
     } else {
-        const int64_t slots = static_cast<int64_t>(sm_count()) * kvq::decode_ctas_per_sm(bf16);
+        const int64_t slots = static_cast<int64_t>(kvq::device_sm_count()) * kvq::decode_ctas_per_sm(bf16);
         const int64_t jobs = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads;
         const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
         want = jobs * big < 4 * slots ? single_wave_splits(jobs, max_ctx, unit, slots, bf16) : 0;
@@ -659,7 +668,7 @@ kvq_status kvq_w4a16_plan(int32_t m, int32_t n, int32_t k, int32_t num_splits, i
         // slots, preferring fewer waves and at least four 256-k blocks per
         // warp (a warp's copies then overlap its arithmetic)
         const int64_t tiles = n / kvq::kW4Cols;
-        const int64_t slots = static_cast<int64_t>(sm_count()) * kvq::w4a16_ctas_per_sm();
+        const int64_t slots = static_cast<int64_t>(kvq::device_sm_count()) * kvq::w4a16_ctas_per_sm();
         double best_score = -1e9;
         for (int s = 1; s <= kvq::kW4MaxSplits; ++s) {
             if (!usable(s) || !runnable(s))

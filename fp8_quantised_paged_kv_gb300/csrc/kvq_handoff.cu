@@ -31,22 +31,6 @@ constexpr int kVecsPerLane = 8;          // 16-byte loads in flight per lane
 constexpr int kCtasPerSmAmax = 8;        // 2,048 threads per SM
 constexpr int kCtasPerSmQuant = 4;       // 1,024 threads per SM (64 registers each)
 
-int device_sms()
-{
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 148;
-    if (dev < 64 && cache[dev] > 0)
-        return cache[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        n = 148;
-    if (dev < 64)
-        cache[dev] = n;
-    return n;
-}
-
 __device__ __forceinline__ float absmax8(uint4 x, float m)
 {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -193,7 +177,7 @@ cudaError_t launch_amax_scales(const HandoffArgs &a, cudaStream_t stream)
     if (a.num_listed > 0) {
         // about kCtasPerSmAmax CTAs per SM in all (one wave), every CTA on one head
         const int heads2 = 2 * a.num_kv_heads;
-        int64_t py = static_cast<int64_t>(device_sms()) * kCtasPerSmAmax / heads2;
+        int64_t py = static_cast<int64_t>(device_sm_count()) * kCtasPerSmAmax / heads2;
         const int64_t most = (a.num_listed + kHandoffWarps - 1) / kHandoffWarps;
         py = py < 1 ? 1 : (py > most ? most : py);
         py = py > 65535 ? 65535 : py;
@@ -212,7 +196,7 @@ cudaError_t launch_quantize_pages(const HandoffArgs &a, cudaStream_t stream)
     const int64_t tiles = 2LL * a.num_kv_heads * a.num_listed;
     if (tiles == 0)
         return cudaSuccess;
-    int64_t blocks = static_cast<int64_t>(device_sms()) * kCtasPerSmQuant;
+    int64_t blocks = static_cast<int64_t>(device_sm_count()) * kCtasPerSmQuant;
     const int64_t need = (tiles + kHandoffWarps - 1) / kHandoffWarps;
     blocks = blocks < need ? blocks : need;
     quantize_pages_kernel<<<static_cast<unsigned>(blocks), kHandoffThreads, 0, stream>>>(a);

@@ -124,4 +124,8 @@ inline int tma_box_rows(int page_size, bool bf16_cache)
 
 cudaError_t read_device_error(uint32_t *bits, bool clear);
 
+// SMs of the current device, queried once per device.  A host with no usable
+// device (the planner's host-only queries) plans for a 152-SM GB300.
+int device_sm_count();
+
 } // namespace kvq

@@ -135,8 +135,8 @@ def test_workspace_too_small_is_reported():
 
 def test_auto_split_fills_the_resident_slots():
     # 8 requests x 8 KV heads at 8,208 tokens: 7 splits fill 448 of the 456
-    # resident CTA slots of a 152-SM part in one wave; a host without a GPU
-    # plans for 148 SMs (444 slots: 6 splits = 384 CTAs, or 7 = 448 in 2 waves)
+    # resident CTA slots of a 152-SM part in one wave (a GB300 itself takes 6,
+    # the most that fit as resident clusters; a host without a GPU has none)
     st, ms, _ = _plan(ps=16, hkv=8, B=8, hq=64, maxp=513)
     assert ms in (6, 7)
     st, ms, _ = _plan(ps=64, hkv=8, B=4, hq=16, maxp=16384)     # long contexts
@@ -165,14 +165,14 @@ def test_w4a16_plan_and_argument_checks():
 
 
 @pytest.mark.parametrize("B,hq,ps,maxp,want", [
-    (8, 64, 16, 513, (1376, 6)),       # uniform8: six splits fill one wave
+    (8, 64, 16, 513, (1184, 7)),       # uniform8: seven splits fill one wave of 456 slots
     (64, 32, 64, 511, (4096, 8)),      # ragged64: 4-8 waves at the longest context -> halved splits
     (4, 16, 64, 16384, (8192, 128)),   # long4: >= 8 waves -> 8,192-token splits
     (32, 32, 16, 257, (4128, 1)),      # 32 x 4,097: one split beats a workspace combine
     (64, 32, 16, 129, (1056, 2)),      # 64 x 2,049: no one-wave plan -> wave-filling rule
 ])
 def test_planner_choices_on_a_host_without_a_gpu(B, hq, ps, maxp, want):
-    """The planner's automatic choices with the host fallback (148 SMs, no
-    clusters): the wave rules for long jobs and the one-wave estimate."""
+    """The planner's automatic choices with the host fallback (a 152-SM GB300,
+    no clusters): the wave rules for long jobs and the one-wave estimate."""
     st, ms, _ = _plan(ps=ps, hkv=8, B=B, hq=hq, maxp=maxp)
     assert (st, ms) == want
