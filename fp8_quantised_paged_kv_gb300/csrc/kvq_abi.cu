@@ -15,16 +15,20 @@ int device_sm_count()
     constexpr int kHostFallbackSms = 152;
     static std::atomic<int> cache[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();                     // leave no error for a later launch check
         return kHostFallbackSms;
+    }
     if (dev >= 0 && dev < 64) {
         const int c = cache[dev].load(std::memory_order_relaxed);
         if (c > 0)
             return c;
     }
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
         n = kHostFallbackSms;
+    }
     if (dev >= 0 && dev < 64)
         cache[dev].store(n, std::memory_order_relaxed);
     return n;
