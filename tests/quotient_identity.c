@@ -28,16 +28,24 @@ static float corrected_quotient(float x, float s, float rcp)
     const float lim = 1024.0f * s;
     const float xc = max_nan(min_nan(x, lim), -lim);
     const float q0 = xc * rcp;
+#ifdef QI_DROP_CORRECTION   /* a planted mistake: the check must then fail */
+    return q0;
+#else
     const float r = fmaf(s, q0, -xc);
     return fmaf(r, -rcp, q0);
+#endif
 }
+
+#ifndef QI_SCALE_SIGNIFICANDS
+#define QI_SCALE_SIGNIFICANDS (1u << 23)
+#endif
 
 int main(void)
 {
     long n = 0, bad = 0;
     for (uint32_t xm = 0; xm < 128; ++xm) {
         const float x = from_bits(0x3F800000u | (xm << 16));
-        for (uint32_t sm = 0; sm < (1u << 23); ++sm) {
+        for (uint32_t sm = 0; sm < QI_SCALE_SIGNIFICANDS; ++sm) {
             const float s = from_bits(0x3F800000u | sm);
             const float q = corrected_quotient(x, s, 1.0f / s);
             ++n;
