@@ -122,6 +122,22 @@ def test_round_trip_and_ties():
     assert np.array_equal(got, expect)
 
 
+def test_one_ulp_either_side_of_every_midpoint():
+    """fp32 values one ulp above / below each midpoint between neighbouring
+    positive codes round up / down (bits far below bf16 precision decide),
+    with either sign."""
+    pos = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    lo = np.arange(0x7E, dtype=np.uint8)
+    above = np.nextafter(mids, np.float32(np.inf))
+    below = np.nextafter(mids, np.float32(0))
+    assert np.array_equal(oracle.e4m3_encode(above), lo + 1)
+    assert np.array_equal(oracle.e4m3_encode(below), lo)
+    assert np.array_equal(oracle.e4m3_encode(-above), (lo + 1) | 0x80)
+    assert np.array_equal(oracle.e4m3_encode(-below), lo | 0x80)
+    assert np.array_equal(oracle.e4m3_encode(above), brute_force_encode(above))
+
+
 @pytest.mark.parametrize("y,code", [
     (448.0, 0x7E), (463.99, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (np.inf, 0x7E),
     (-np.inf, 0xFE), (-500.0, 0xFE), (0.0, 0x00), (-0.0, 0x80),
