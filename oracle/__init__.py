@@ -74,6 +74,9 @@ def _load():
     lib.oracle_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P,
                                        P, i32, P, ctypes.c_float, P, P]
     lib.oracle_decode_attn.restype = None
+    lib.oracle_decode_attn_multi.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, P, P, P,
+                                             P, P, P, i32, P, ctypes.c_float, P, P]
+    lib.oracle_decode_attn_multi.restype = None
     lib.oracle_amax_scales.argtypes = [i32, i32, i32, P, P, P, i32, P, P]
     lib.oracle_amax_scales.restype = None
     lib.oracle_quantize_pages.argtypes = [i32, i32, i32, P, P, P, P, P, P, i32, P, P]
@@ -183,6 +186,36 @@ def decode_attn(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
     lib.oracle_decode_attn(B, Hq, Hkv, D, ps, N, int(is_bf16), _ptr(q), _ptr(k_cache),
                            _ptr(v_cache), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
                            _ptr(sl), ctypes.c_float(softmax_scale), _ptr(ab), _ptr(out))
+    return out
+
+
+def decode_attn_multi(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                      softmax_scale: float, abort_flags=None) -> np.ndarray:
+    """fp64 multi-token decode attention; returns float64 [B][n][Hq][D].
+
+    ``q`` is uint16 bf16 bits [B][n][Hq][D]: n new query tokens per request,
+    the request's last n positions (seq_lens count them).  Query token i of
+    request r attends causally to positions 0 .. seq_lens[r] - n + i; a query
+    with no position to attend to, and every query of a request the
+    single-token attention zeroes, gives zeros.
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, n, Hq, D = q.shape
+    is_bf16 = k_cache.dtype == np.uint16
+    N, Hkv, ps, D2 = k_cache.shape
+    assert D2 == D and Hq % Hkv == 0
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ks = _c(k_scale, np.float32) if k_scale is not None else np.ones(Hkv, np.float32)
+    vs = _c(v_scale, np.float32) if v_scale is not None else np.ones(Hkv, np.float32)
+    ab = None if abort_flags is None else _c(abort_flags, np.uint8)
+    out = np.empty((B, n, Hq, D), np.float64)
+    lib.oracle_decode_attn_multi(B, n, Hq, Hkv, D, ps, N, int(is_bf16), _ptr(q), _ptr(k_cache),
+                                 _ptr(v_cache), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
+                                 _ptr(sl), ctypes.c_float(softmax_scale), _ptr(ab), _ptr(out))
     return out
 
 

@@ -305,6 +305,91 @@ void oracle_decode_attn(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads
     }
 }
 
+/*
+ * Multi-token decode (several new query tokens per request, as in verifying
+ * speculative drafts): the pages say nothing about it; the reading taken is
+ * that the n new tokens are the request's last n positions, already in the
+ * cache, and that each attends causally -- query token i of request r, at
+ * position L_r - n + i, attends to positions 0 .. L_r - n + i, every one of
+ * them through the block table, exactly as oracle_decode_attn attends a
+ * single query to positions 0 .. L_r - 1.  A query with no position to
+ * attend to (L_r - n + i < 0) gets zeros; so does every query of a request
+ * that oracle_decode_attn would zero (aborted, empty, longer than its table,
+ * or naming a page outside [0, num_pages)).
+ *   q, out   [B][n_query][Hq][D] (bf16 bits in, fp64 out).
+ */
+void oracle_decode_attn_multi(int32_t batch, int32_t n_query, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                              int32_t num_pages, int32_t cache_is_bf16, const uint16_t *q,
+                              const void *k_cache, const void *v_cache,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *block_table, int32_t max_pages_per_seq,
+                              const int32_t *seq_lens, float softmax_scale,
+                              const uint8_t *abort_flags, double *out)
+{
+    const int32_t group = num_q_heads / num_kv_heads;
+    const double sigma = (double)softmax_scale;
+    int64_t rih;
+    const int64_t total = (int64_t)batch * n_query * num_q_heads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (rih = 0; rih < total; ++rih) {
+        const int32_t r = (int32_t)(rih / ((int64_t)n_query * num_q_heads));
+        const int32_t i = (int32_t)((rih / num_q_heads) % n_query);
+        const int32_t h = (int32_t)(rih % num_q_heads);
+        double *o = out + rih * head_dim;
+        for (int32_t d = 0; d < head_dim; ++d)
+            o[d] = 0.0;
+        const int64_t len = seq_lens[r];
+        if (len <= 0 || (abort_flags && abort_flags[r]))
+            continue;
+        const int64_t used = (len + page_size - 1) / page_size;
+        if (used > max_pages_per_seq)
+            continue;
+        const int32_t *row = block_table + (int64_t)r * max_pages_per_seq;
+        int valid = 1;
+        for (int64_t p = 0; p < used; ++p)
+            if (row[p] < 0 || row[p] >= num_pages)
+                valid = 0;
+        if (!valid)
+            continue;
+        /* positions this query sees: 0 .. len - n_query + i */
+        const int64_t seen = len - n_query + i + 1;
+        if (seen <= 0)
+            continue;
+
+        const int32_t kvh = h / group;
+        const double ks = cache_is_bf16 ? 1.0 : (double)k_scale[kvh];
+        const double vs = cache_is_bf16 ? 1.0 : (double)v_scale[kvh];
+        const uint16_t *qh = q + rih * head_dim;
+        double *s = (double *)malloc((size_t)seen * sizeof(double));
+        double smax = -INFINITY;
+        for (int64_t j = 0; j < seen; ++j) {
+            int64_t base = (((int64_t)row[j / page_size] * num_kv_heads + kvh) * page_size
+                            + j % page_size) * head_dim;
+            double dot = 0.0;
+            for (int32_t d = 0; d < head_dim; ++d)
+                dot += bf16_bits_to_double(qh[d]) * cache_value(k_cache, cache_is_bf16, base + d, ks);
+            s[j] = sigma * dot;
+            if (s[j] > smax)
+                smax = s[j];
+        }
+        double den = 0.0;
+        for (int64_t j = 0; j < seen; ++j) {
+            double w = exp(s[j] - smax);
+            int64_t base = (((int64_t)row[j / page_size] * num_kv_heads + kvh) * page_size
+                            + j % page_size) * head_dim;
+            den += w;
+            for (int32_t d = 0; d < head_dim; ++d)
+                o[d] += w * cache_value(v_cache, cache_is_bf16, base + d, vs);
+        }
+        for (int32_t d = 0; d < head_dim; ++d)
+            o[d] /= den;
+        free(s);
+    }
+}
+
 /* Threads the attention loop runs on (1 without OpenMP). */
 int32_t oracle_num_threads(void)
 {
