@@ -10,6 +10,7 @@ missing the calls raise.
     kvq_append(...)         quantise-on-append of new K/V into paged slots
     kvq_decode_attn(...)    split-K paged decode attention + LSE combine
     kvq_decode_plan(...)    split / workspace sizes for kvq_decode_attn
+    kvq_decode_attn_mt(...), kvq_decode_plan_mt(...)   several new query tokens per request
     kvq_decode_attn_append(...), kvq_tag_check_append(...)   fused forms
     kvq_decode_step(...)    tag check + append + attention of a decode step, one launch
     kvq_amax_scales(...), kvq_quantize_pages(...)            prefill -> decode handoff
@@ -73,6 +74,10 @@ _SIGS = {
     "kvq_read_probe": ["p", "size", "p", "p"],
     "kvq_w4a16_gemm": ["p", "p", "p", "i32", "i32", "i32", "p", "i32", "i32", "p"],
     "kvq_device_error": ["p", "i32"],
+    "kvq_diag_set_copy_wait_ns": ["i64"],
+    "kvq_decode_plan_mt": ["desc", "i32", "i32", "i32", "i32", "i32", "p", "p", "p"],
+    "kvq_decode_attn_mt": ["desc", "p", "i32", "i32", "i32", "p", "p", "p", "p", "p", "i32", "p", "f32",
+                           "p", "p", "i32", "p", "size", "i32", "p"],
     "kvq_amax_scales": ["desc", "p", "p", "p", "i32", "p", "p", "p"],
     "kvq_quantize_pages": ["desc", "p", "p", "p", "desc", "p", "p", "p", "i32", "p", "p", "p"],
     "kvq_tag_check_append": ["desc", "p", "p", "p", "i32", "i32", "p", "p", "p", "p", "p", "p",
@@ -93,7 +98,7 @@ def load(path: str | None = None):
         build()
     lib = ctypes.CDLL(path)
     T = {"p": ctypes.c_void_p, "i32": ctypes.c_int32, "f32": ctypes.c_float,
-         "size": ctypes.c_size_t, "desc": ctypes.POINTER(_Desc)}
+         "size": ctypes.c_size_t, "desc": ctypes.POINTER(_Desc), "i64": ctypes.c_int64}
     for name, sig in _SIGS.items():
         fn = getattr(lib, name)
         fn.argtypes = [T[s] for s in sig]
@@ -226,6 +231,26 @@ def kvq_decode_plan(desc: CacheDesc, batch: int, num_q_heads: int, max_pages_per
     return a.value, b.value, c.value
 
 
+def kvq_decode_plan_mt(desc: CacheDesc, batch: int, num_query_tokens: int, num_q_heads: int,
+                       max_pages_per_seq: int, num_splits: int = 0):
+    """(split_tokens, max_splits, workspace_bytes) that kvq_decode_attn_mt will use."""
+    a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    st = load().kvq_decode_plan_mt(ctypes.byref(desc.c()), batch, num_query_tokens, num_q_heads,
+                                   max_pages_per_seq, num_splits, ctypes.byref(a), ctypes.byref(b),
+                                   ctypes.byref(c))
+    _check("kvq_decode_plan_mt", st)
+    return a.value, b.value, c.value
+
+
+def workspace_for_mt(desc: CacheDesc, batch, num_query_tokens, num_q_heads, max_pages_per_seq,
+                     num_splits=0, device="cuda"):
+    """Allocate (with torch) the zero-filled workspace of a multi-token decode call."""
+    import torch
+    nbytes = kvq_decode_plan_mt(desc, batch, num_query_tokens, num_q_heads, max_pages_per_seq,
+                                num_splits)[2]
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
 def workspace_for(desc: CacheDesc, batch, num_q_heads, max_pages_per_seq, num_splits=0, device="cuda"):
     """Allocate (with torch) the zero-filled decode workspace the plan asks for."""
     import torch
@@ -260,6 +285,29 @@ def kvq_decode_attn(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, se
     """Paged decode attention into ``out`` (bf16 or fp32 [B][Hq][D])."""
     return _decode("kvq_decode_attn", desc, q, k_cache, v_cache, k_scale, v_scale, block_table,
                    seq_lens, softmax_scale, abort_flags, out, workspace, num_splits, stream)
+
+
+def kvq_decode_attn_mt(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                       softmax_scale, abort_flags, out, workspace, num_splits=0, stream=None):
+    """Decode attention for n new query tokens per request, causal among them:
+    q bf16 [B][n][Hq][D] into ``out`` (bf16 or fp32 [B][n][Hq][D])."""
+    import torch
+    B, n, Hq, D = q.shape
+    _expect(q, torch.bfloat16, (B, n, Hq, desc.head_dim), "q")
+    _expect(block_table, torch.int32, None, "block_table")
+    _expect(seq_lens, torch.int32, (B,), "seq_lens")
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (B, n, Hq, D):
+        raise ValueError("out: expected bf16 or fp32 [B][n][Hq][D]")
+    out_dtype = KVQ_OUT_FP32 if out.dtype == torch.float32 else KVQ_OUT_BF16
+    if abort_flags is not None:
+        _expect(abort_flags, torch.uint8, (B,), "abort_flags")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kvq_decode_attn_mt(
+        ctypes.byref(desc.c()), _ptr(q), B, n, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        ctypes.c_float(softmax_scale), _ptr(abort_flags), _ptr(out), out_dtype, _ptr(workspace),
+        ws_bytes, num_splits, _stream(stream))
+    _check("kvq_decode_attn_mt", st)
 
 
 def kvq_decode_attn_append(desc, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
@@ -357,6 +405,12 @@ def kvq_w4a16_gemm(x, w, scales, y, num_splits: int = 0, stream=None):
                                num_splits, _stream(stream))
     _check("kvq_w4a16_gemm", st)
     return y
+
+
+def kvq_diag_set_copy_wait_ns(ns: int) -> None:
+    """Test hook: the decode kernel's limit on each wait for a bulk copy, for
+    later launches (0 = give up at once; negative = the default of about 1 s)."""
+    _check("kvq_diag_set_copy_wait_ns", load().kvq_diag_set_copy_wait_ns(int(ns)))
 
 
 def kvq_device_error(clear: bool = False) -> int:

@@ -12,6 +12,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
+# The same sources built with per-phase %globaltimer stamps in the decode and
+# tag-check kernels (bench.py --phase-stamps); never the product library.
+STAMPS_LIB = os.path.join(BUILD, "libkvq_stamps.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -36,18 +39,22 @@ def _deps():
         + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ in parallel and link libkvq.so."""
-    os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB):
+def build(force: bool = False, verbose: bool = False, stamps: bool = False) -> str:
+    """Compile every .cu under csrc/ in parallel and link libkvq.so (with
+    stamps=True: libkvq_stamps.so, the instrumented variant)."""
+    lib = STAMPS_LIB if stamps else LIB
+    objdir = os.path.join(BUILD, "stamps") if stamps else BUILD
+    os.makedirs(objdir, exist_ok=True)
+    if not force and os.path.exists(lib):
         newest = max(os.path.getmtime(p) for p in _deps())
-        if os.path.getmtime(LIB) >= newest:
-            return LIB
+        if os.path.getmtime(lib) >= newest:
+            return lib
     nvcc = _nvcc()
+    extra = ["-DKVQ_PHASE_STAMPS"] if stamps else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc] + NVCC_FLAGS + ["-c", src, "-o", obj]
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        cmd = [nvcc] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -60,14 +67,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp] + \
         [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -34,6 +34,12 @@ int device_sm_count()
     return n;
 }
 
+namespace {
+std::atomic<uint64_t> g_copy_wait_ns{kCopyWaitLimitNs};
+} // namespace
+
+uint64_t decode_copy_wait_ns() { return g_copy_wait_ns.load(std::memory_order_relaxed); }
+
 } // namespace kvq
 
 namespace {
@@ -67,7 +73,7 @@ kvq_status check_desc(const kvq_cache_desc *d)
 }
 
 struct Plan {
-    int32_t split_tokens, max_splits;
+    int32_t split_tokens, max_splits, row_blocks;
     int32_t cluster;              // 0, or the cluster size (= max_splits) of the cluster combine
     size_t counter_bytes, lse_bytes, o_bytes;
 };
@@ -162,14 +168,21 @@ int64_t single_wave_splits(int64_t pairs, int64_t max_ctx, int64_t unit, int64_t
     return best;
 }
 
+// Query rows of a CTA (one mma n-tile) and the most new query tokens per
+// request a multi-token call takes.
+constexpr int kRowsPerCta = kvq::kMaxGroup;
+constexpr int kMaxQueryTokens = 16;
+
 kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads,
-                     int32_t max_pages, int32_t num_splits, Plan *p)
+                     int32_t max_pages, int32_t num_splits, Plan *p, int32_t n_query = 1)
 {
     kvq_status st = check_desc(d);
     if (st != KVQ_OK)
         return st;
-    if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0)
+    if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0 || n_query < 1)
         return KVQ_ERR_INVALID_ARG;
+    if (n_query > kMaxQueryTokens)
+        return KVQ_ERR_UNSUPPORTED;
     if (batch > 65535)
         return KVQ_ERR_UNSUPPORTED;
     if (num_q_heads % d->num_kv_heads != 0)
@@ -180,14 +193,19 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     const int64_t max_ctx = static_cast<int64_t>(max_pages) * d->page_size;
     const int64_t unit = d->page_size > kChunkTokens ? d->page_size : kChunkTokens;
     const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
-    const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads;
+    // CTAs per split: one per (request, KV head, block of 8 query rows)
+    const int64_t row_blocks = (static_cast<int64_t>(n_query) * g + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads * row_blocks;
+    p->row_blocks = static_cast<int32_t>(row_blocks);
+    if (static_cast<int64_t>(d->num_kv_heads) * row_blocks > 65535)
+        return KVQ_ERR_UNSUPPORTED;                  // the grid's second dimension
     int64_t want;
     bool single_wave = false;
     if (num_splits > 0) {
         want = num_splits;
     } else {
         const int64_t slots = static_cast<int64_t>(kvq::device_sm_count()) * kvq::decode_ctas_per_sm(bf16);
-        const int64_t jobs = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads;
+        const int64_t jobs = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads * row_blocks;
         const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
         want = jobs * big < 4 * slots ? single_wave_splits(jobs, max_ctx, unit, slots, bf16) : 0;
         single_wave = want > 0;
@@ -222,11 +240,11 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (splits >= 2 && batch > 0 &&
         pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16))
         p->cluster = static_cast<int32_t>(splits);
-    p->counter_bytes = (static_cast<size_t>(batch) * d->num_kv_heads * 4 + 255) / 256 * 256;
+    p->counter_bytes = (static_cast<size_t>(pairs) * 4 + 255) / 256 * 256;
     if (p->counter_bytes == 0)
         p->counter_bytes = 256;
     if (splits > 1 && p->cluster == 0) {
-        const size_t n = static_cast<size_t>(batch) * num_q_heads * splits;
+        const size_t n = static_cast<size_t>(batch) * n_query * num_q_heads * splits;
         p->lse_bytes = (n * sizeof(float) + 255) / 256 * 256;
         p->o_bytes = n * kHeadDim * sizeof(float);
     } else {
@@ -291,9 +309,10 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
                           int32_t max_pages_per_seq, const int32_t *seq_lens, float softmax_scale,
                           const uint8_t *abort_flags, void *out, int32_t out_dtype,
                           void *workspace, size_t workspace_bytes, int32_t num_splits,
-                          DecodeCall *call)
+                          DecodeCall *call, int32_t n_query = 1)
 {
-    kvq_status st = make_plan(desc, batch, num_q_heads, max_pages_per_seq, num_splits, &call->plan);
+    kvq_status st = make_plan(desc, batch, num_q_heads, max_pages_per_seq, num_splits, &call->plan,
+                              n_query);
     if (st != KVQ_OK)
         return st;
     if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_FP32)
@@ -341,7 +360,10 @@ kvq_status prepare_decode(const kvq_cache_desc *desc, const void *q, int32_t bat
     a.split_tokens = call->plan.split_tokens;
     a.max_splits = call->plan.max_splits;
     a.cluster = call->plan.cluster;
+    a.n_query = n_query;
+    a.row_blocks = call->plan.row_blocks;
     a.qk_scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.copy_wait_ns = kvq::decode_copy_wait_ns();
     a.out_fp32 = out_dtype == KVQ_OUT_FP32;
     a.bf16_cache = bf16;
     return KVQ_OK;
@@ -577,6 +599,46 @@ kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, int32_t ba
     return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_decode_plan_mt(const kvq_cache_desc *desc, int32_t batch, int32_t num_query_tokens,
+                              int32_t num_q_heads, int32_t max_pages_per_seq, int32_t num_splits,
+                              int32_t *split_tokens, int32_t *max_splits, size_t *workspace_bytes)
+{
+    Plan p;
+    kvq_status st = make_plan(desc, batch, num_q_heads, max_pages_per_seq, num_splits, &p,
+                              num_query_tokens);
+    if (st != KVQ_OK)
+        return st;
+    if (split_tokens)
+        *split_tokens = p.split_tokens;
+    if (max_splits)
+        *max_splits = p.max_splits;
+    if (workspace_bytes)
+        *workspace_bytes = p.counter_bytes + p.lse_bytes + p.o_bytes;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn_mt(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                              int32_t num_query_tokens, int32_t num_q_heads, const void *k_cache,
+                              const void *v_cache, const float *k_scale, const float *v_scale,
+                              const int32_t *block_table, int32_t max_pages_per_seq,
+                              const int32_t *seq_lens, float softmax_scale,
+                              const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                              void *workspace, size_t workspace_bytes, int32_t num_splits,
+                              kvq_stream_t stream)
+{
+    DecodeCall call;
+    kvq_status st = prepare_decode(desc, q, batch, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                   block_table, max_pages_per_seq, seq_lens, softmax_scale,
+                                   abort_flags, out, out_dtype, workspace, workspace_bytes,
+                                   num_splits, &call, num_query_tokens);
+    if (st != KVQ_OK || batch == 0)
+        return st;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
+        return KVQ_ERR_CUDA;
+    return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_decode_attn_append(const kvq_cache_desc *desc, const void *q, int32_t batch,
                                   int32_t num_q_heads, void *k_cache, void *v_cache,
                                   const float *k_scale, const float *v_scale,
@@ -635,6 +697,28 @@ kvq_status kvq_decode_step(const kvq_cache_desc *desc, const void *q, int32_t ba
         return KVQ_ERR_CUDA;
     return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
 }
+
+kvq_status kvq_diag_set_copy_wait_ns(int64_t ns)
+{
+    const uint64_t v = ns < 0 || static_cast<uint64_t>(ns) > kvq::kCopyWaitLimitNs
+                           ? kvq::kCopyWaitLimitNs
+                           : static_cast<uint64_t>(ns);
+    kvq::g_copy_wait_ns.store(v, std::memory_order_relaxed);
+    return KVQ_OK;
+}
+
+#ifdef KVQ_PHASE_STAMPS
+// Instrumented build only (no declaration in the public header): copy the
+// phase stamps of the last launch to host memory.  which = 0: decode kernel,
+// [CTA][8]; 1: tag check + append kernel, [CTA][2].
+KVQ_API kvq_status kvq_phase_stamps(int32_t which, unsigned long long *host, size_t count)
+{
+    if (host == nullptr)
+        return KVQ_ERR_INVALID_ARG;
+    return to_status(which == 0 ? kvq::read_decode_stamps(host, count)
+                                : kvq::read_check_stamps(host, count));
+}
+#endif
 
 kvq_status kvq_device_error(uint32_t *bits, int32_t clear)
 {

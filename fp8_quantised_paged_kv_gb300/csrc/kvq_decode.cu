@@ -37,8 +37,34 @@
 
 namespace kvq {
 
-// Sticky device error word (bit 0: a bulk-copy wait timed out).
+// Sticky device error word.  Bit 0: a bulk-copy wait timed out.  Bit 1: the
+// drain that follows also gave up, so a copy may still land in the shared
+// memory the CTA leaves behind.
 __device__ unsigned int g_device_error = 0;
+
+#ifdef KVQ_PHASE_STAMPS
+// Instrumented build only (-DKVQ_PHASE_STAMPS, a library of its own): thread
+// 0 of every CTA of a decode launch records %globaltimer at fixed points;
+// the host clears them before each launch and reads them back.  Points:
+// 0 entry, 1 the programmatic-launch wait returned, 2 warp 0's first chunk
+// landed, 3 every warp done streaming, 4 in-CTA merge done, 5 the combine's
+// first synchronisation passed (cluster barrier or arrival counter),
+// 6 exit of a CTA that streamed.
+constexpr int kStampCtas = 8192;
+constexpr int kStampPoints = 8;
+__device__ unsigned long long g_phase_stamps[kStampCtas * kStampPoints];
+__device__ __forceinline__ void phase_stamp(int point)
+{
+    if (threadIdx.x == 0) {
+        const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        if (cta < kStampCtas)
+            g_phase_stamps[cta * kStampPoints + point] = global_timer_ns();
+    }
+}
+#define KVQ_STAMP(p) phase_stamp(p)
+#else
+#define KVQ_STAMP(p) ((void)0)
+#endif
 
 namespace {
 
@@ -46,7 +72,6 @@ constexpr int kWarps = 4;
 constexpr int kCtasPerSm = 3;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // give up on a copy after ~1 s
 constexpr int kPrefetchTokens = 256;             // per split, requested into L2 before the wait
 // Published lse of a split that has no result: both are NaN, so the combine
 // zeroes the request either way; the payload tells a failed tag check (the
@@ -72,6 +97,21 @@ struct Tile {
 __device__ __forceinline__ uint32_t swz(int line, int c)
 {
     return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
+}
+
+// The exponent e that puts a row's largest magnitude, given as the bf16 bits
+// `mx` of |q| (sign cleared), in [2^14, 2^15): e = 14 - floor(log2 |q|max),
+// at most 100 (a row below 2^-86 is scaled up less; its scores are that much
+// closer to 0 anyway), so that 2^e and 2^-e are normal fp32 numbers (e is at
+// least -113 for finite bf16).  A row of zeros keeps e = 0.
+__device__ __forceinline__ int row_pow2_exponent(uint32_t mx)
+{
+    if (mx == 0)
+        return 0;
+    const int field = static_cast<int>(mx >> 7);           // biased exponent (no sign bit)
+    const int e_floor = field != 0 ? field - 127 : (31 - __clz(static_cast<int>(mx))) - 133;
+    const int e = 14 - e_floor;
+    return e > 100 ? 100 : e;
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t *base, uint32_t off)
@@ -104,6 +144,24 @@ __device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool 
         static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
 }
 
+
+// The query rows one CTA serves.  The rows of (request b, KV head kvh) are
+// (token i, head h) for the request's n_query new tokens and the g query
+// heads of the group, row i * g + h; a CTA takes rows row0 .. row0 + nrows - 1
+// (at most kMaxGroup: one mma n-tile).  With one query token the rows are
+// the group's heads and one CTA takes them all.
+struct Rows {
+    int b, kvh, row0, nrows;
+    int64_t slot;                            // this (request, KV head, row block)'s arrival counter
+
+    // Row of q and out ([B][n_query][Hq][D], in units of head_dim) of local row r.
+    __device__ int64_t id(const DecodeArgs &a, int r) const
+    {
+        const int rr = row0 + r;
+        return (static_cast<int64_t>(b) * a.n_query + rr / a.group) * a.num_q_heads + kvh * a.group +
+               rr % a.group;
+    }
+};
 
 // The warps' merge area holds one row of 128 floats per (warp, head).  Row
 // stride and a skew of 2 words per 32 dims make the fragment stores (a lane
@@ -157,7 +215,7 @@ __device__ void finish_step(const DecodeArgs &a, int b, int kvh, bool stale)
     }
 }
 
-__device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsplit, float *scratch)
+__device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nsplit, float *scratch)
 {
     __shared__ int s_last;
     // The block barrier orders every thread's partial before thread 0's
@@ -165,18 +223,18 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
     // peers' partials before its loads (the counter is the only
     // synchronisation between the splits).
     __syncthreads();
-    unsigned int *counter = a.counters + static_cast<int64_t>(b) * a.num_kv_heads + kvh;
+    unsigned int *counter = a.counters + R.slot;
     if (threadIdx.x == 0)
         s_last = atom_add_acq_rel_gpu(counter, 1u) == static_cast<unsigned int>(nsplit - 1);
     __syncthreads();
+    KVQ_STAMP(5);
     if (!s_last)
         return;
-    const int g = a.group, n = nsplit;
-    const int64_t bh0 = static_cast<int64_t>(b) * a.num_q_heads + kvh * g;
-    float *s_tot = scratch;                  // [8] sum of weights (0: drop the head)
+    const int g = R.nrows, n = nsplit;
+    float *s_tot = scratch;                  // [8] sum of weights (0: drop the row)
     float *s_w = scratch + kMaxGroup;        // [g][n]: lse, then weights
     for (int i = threadIdx.x; i < g * n; i += kThreads)
-        s_w[i] = __ldcg(a.ws_lse + (bh0 + i / n) * a.max_splits + i % n);
+        s_w[i] = __ldcg(a.ws_lse + R.id(a, i / n) * a.max_splits + i % n);
     __syncthreads();
     // one warp per head: max, validity, weights, their sum
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -192,8 +250,8 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
         for (int off = 16; off > 0; off >>= 1)
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
         float sum = 0.f;
-        for (int s = lane; s < n; s += 32) {
-            const float e = bad ? 0.f : fast_exp2(w[s] - m);
+        for (int s = lane; s < n; s += 32) {         // a split that saw no token: lse -inf, weight 0
+            const float e = (bad || w[s] == -INFINITY) ? 0.f : fast_exp2(w[s] - m);
             w[s] = e;
             sum += e;
         }
@@ -219,7 +277,7 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
             for (int j = 0; j < kRound; ++j)
                 v[q][j] = (hp[q] < g && s0 + j < n)
                               ? __ldcg(reinterpret_cast<const float4 *>(
-                                    a.ws_o + ((bh0 + hp[q]) * a.max_splits + s0 + j) * kHeadDim + cp))
+                                    a.ws_o + (R.id(a, hp[q]) * a.max_splits + s0 + j) * kHeadDim + cp))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
@@ -236,7 +294,7 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
 #pragma unroll
     for (int q = 0; q < 2; ++q)
         if (hp[q] < g) {
-            const int64_t o0 = (bh0 + hp[q]) * kHeadDim + cp;
+            const int64_t o0 = R.id(a, hp[q]) * kHeadDim + cp;
             store_out(a.out, o0, s_tot[hp[q]] > 0.f ? acc[q].x / s_tot[hp[q]] : 0.f, a.out_fp32);
             store_out(a.out, o0 + 1, s_tot[hp[q]] > 0.f ? acc[q].y / s_tot[hp[q]] : 0.f, a.out_fp32);
             store_out(a.out, o0 + 2, s_tot[hp[q]] > 0.f ? acc[q].z / s_tot[hp[q]] : 0.f, a.out_fp32);
@@ -247,11 +305,11 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
         if (threadIdx.x == 0) {
             int any = 0;
             for (int sp = 0; sp < n; ++sp)
-                any |= __float_as_uint(__ldcg(a.ws_lse + bh0 * a.max_splits + sp)) == kLseStale;
+                any |= __float_as_uint(__ldcg(a.ws_lse + R.id(a, 0) * a.max_splits + sp)) == kLseStale;
             s_stale_any = any;
         }
         __syncthreads();
-        finish_step(a, b, kvh, s_stale_any != 0);
+        finish_step(a, R.b, R.kvh, s_stale_any != 0);
     }
     if (threadIdx.x == 0)
         *counter = 0;                        // ready for the next call
@@ -260,22 +318,19 @@ __device__ void publish_and_combine(const DecodeArgs &a, int b, int kvh, int nsp
 // A split that cannot produce a result (invalid page id, or a copy that
 // timed out): a single-split request gets zeros; otherwise the split
 // publishes an invalid (NaN) lse so the combine zeroes the request.
-__device__ void drop_split(const DecodeArgs &a, int b, int kvh, int split, int nsplit, float *smem,
+__device__ void drop_split(const DecodeArgs &a, const Rows &R, int split, int nsplit, float *smem,
                            uint32_t lse_bits = kLseInvalid)
 {
-    const int hq0 = kvh * a.group;
     if (nsplit == 1) {
-        for (int i = threadIdx.x; i < a.group * kHeadDim; i += kThreads)
-            store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + hq0) * kHeadDim + i, 0.f,
-                      a.out_fp32);
+        for (int i = threadIdx.x; i < R.nrows * kHeadDim; i += kThreads)
+            store_out(a.out, R.id(a, i / kHeadDim) * kHeadDim + i % kHeadDim, 0.f, a.out_fp32);
         if (a.expected_tags != nullptr)
-            finish_step(a, b, kvh, lse_bits == kLseStale);
+            finish_step(a, R.b, R.kvh, lse_bits == kLseStale);
         return;
     }
-    if (threadIdx.x < a.group)
-        a.ws_lse[(static_cast<int64_t>(b) * a.num_q_heads + hq0 + threadIdx.x) * a.max_splits + split] =
-            __uint_as_float(lse_bits);
-    publish_and_combine(a, b, kvh, nsplit, smem + kScratchOffset);
+    if (threadIdx.x < R.nrows)
+        a.ws_lse[R.id(a, threadIdx.x) * a.max_splits + split] = __uint_as_float(lse_bits);
+    publish_and_combine(a, R, nsplit, smem + kScratchOffset);
 }
 
 // What a split contributes to the cluster form of the combine.
@@ -295,7 +350,7 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPa
 // same `finisher`: for kvq_decode_step the rank that reads every peer's
 // verdict, else -1.  Returns, on the finisher, whether any split of the
 // request failed its tag check (false elsewhere).
-__device__ bool cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatus status, float *part,
+__device__ bool cluster_finish(const DecodeArgs &a, const Rows &R, PartialStatus status, float *part,
                                int finisher)
 {
     __shared__ int s_any_stale;
@@ -303,7 +358,8 @@ __device__ bool cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
         part[threadIdx.x] = status == kPartialEmpty ? -INFINITY
                             : __uint_as_float(status == kPartialStale ? kLseStale : kLseInvalid);
     cluster_sync();
-    const int g = a.group, n = a.max_splits;
+    KVQ_STAMP(5);
+    const int g = R.nrows, n = a.max_splits;
     const int rank = static_cast<int>(cluster_ctarank());
     const uint32_t base = smem_addr(part);
     if (rank == finisher && threadIdx.x == 0) {            // every peer's head-0 lse carries its verdict
@@ -353,7 +409,7 @@ __device__ bool cluster_finish(const DecodeArgs &a, int b, int kvh, PartialStatu
             }
         }
         const bool zero = bad || !(sum > 0.f);
-        const int64_t o0 = (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * kHeadDim + d;
+        const int64_t o0 = R.id(a, h) * kHeadDim + d;
         store_out(a.out, o0, zero ? 0.f : acc.x / sum, a.out_fp32);
         store_out(a.out, o0 + 1, zero ? 0.f : acc.y / sum, a.out_fp32);
         store_out(a.out, o0 + 2, zero ? 0.f : acc.z / sum, a.out_fp32);
@@ -369,6 +425,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a)
 {
     using T = Tile<kBf16Cache>;
+    KVQ_STAMP(0);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -380,11 +437,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     __shared__ int s_failed;
     __shared__ int s_stale;                                // kvq_decode_step: a page of this split failed
 
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int kvh = static_cast<int>(blockIdx.y) / a.row_blocks;
+    const int rb = static_cast<int>(blockIdx.y) % a.row_blocks;   // block of 8 query rows
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gq = lane >> 2, tq = lane & 3;
     const int g = a.group, ps = a.page_size;
-    const int hq0 = kvh * g;                               // first query head of the group
+    Rows R;
+    R.b = b;
+    R.kvh = kvh;
+    R.row0 = rb * kMaxGroup;
+    R.nrows = min(kMaxGroup, a.n_query * g - R.row0);
+    R.slot = static_cast<int64_t>(b) * gridDim.y + blockIdx.y;
 
     const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
     const int span_left = a.max_pages_per_seq - first_page;
@@ -404,7 +468,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         prefetch_tensor_map(&k_map);
         prefetch_tensor_map(&v_map);
     }
-    {
+    if (rb == 0) {                                         // the other row blocks read the same pages
         const int box_tok = ps < kChunkTokens ? ps : kChunkTokens;
         const int boxes = kPrefetchTokens / box_tok;
         for (int i = threadIdx.x; i < boxes; i += kThreads) {
@@ -422,6 +486,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         }
     }
     grid_dependency_wait();
+    KVQ_STAMP(1);
 
     // The block-table entries this split can use depend only on the split
     // index, so they are loaded together with the request's length.
@@ -455,7 +520,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int finisher = step_check && !zero_request ? nsplit - 1 : -1;
     if constexpr (kCluster) {
         if (zero_request || split >= nsplit) {             // no tokens: weight 0
-            cluster_finish(a, b, kvh, kPartialEmpty, part, finisher);
+            cluster_finish(a, R, kPartialEmpty, part, finisher);
             return;
         }
     }
@@ -463,9 +528,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         return;
 
     if (zero_request) {                                    // split 0 writes the zeros
-        for (int i = threadIdx.x; i < g * kHeadDim; i += kThreads)
-            store_out(a.out, (static_cast<int64_t>(b) * a.num_q_heads + hq0) * kHeadDim + i, 0.f,
-                      a.out_fp32);
+        for (int i = threadIdx.x; i < R.nrows * kHeadDim; i += kThreads)
+            store_out(a.out, R.id(a, i / kHeadDim) * kHeadDim + i % kHeadDim, 0.f, a.out_fp32);
         return;
     }
 
@@ -556,11 +620,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 
     if (bad) {                                             // for kvq_decode_step a failed check
         if constexpr (kCluster) {
-            cluster_finish(a, b, kvh, step_check ? kPartialStale : kPartialInvalid, part, finisher);
+            cluster_finish(a, R, step_check ? kPartialStale : kPartialInvalid, part, finisher);
             if (split == finisher)                         // this split failed: so did the request
                 finish_here(true);
         } else
-            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem),
+            drop_split(a, R, split, nsplit, reinterpret_cast<float *>(smem),
                        step_check ? kLseStale : kLseInvalid);
         return;
     }
@@ -573,7 +637,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int box_tok = ps < kChunkTokens ? ps : kChunkTokens;
     const int parts = kChunkTokens / box_tok;                       // 1 or 2 copies per tensor
     const uint32_t part_bytes = static_cast<uint32_t>(box_tok * T::kRowBytes);
-    const uint64_t policy = l2_policy_evict_first();
+    // evict-first unless other row blocks of the split read the same pages
+    const uint64_t policy = a.row_blocks > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
 
 
     // Issue the copies of this warp's local chunk `it` (lane 0 only).
@@ -623,16 +688,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         cp_async_commit();
     }
 
-    // Query fragments (mma B operand): lane (gq, tq) holds query head gq of
-    // the group at dims 32*tq .. 32*tq+31; k-slot pairs of k-step c map to
-    // dims 32*tq + 4*c + {0,1} and {2,3}.
+    // Query fragments (mma B operand): lane (gq, tq) holds query row gq of
+    // this CTA (with one query token: head gq of the group) at dims 32*tq ..
+    // 32*tq+31; k-slot pairs of k-step c map to dims 32*tq + 4*c + {0,1} and
+    // {2,3}.
+    //
+    // FP8 cache: the product runs in f16, whose range is narrower than
+    // bf16's.  Each q row is first multiplied by 2^e_h, the power of two that
+    // puts its largest magnitude in [2^14, 2^15) (exact: only the exponent
+    // changes), so no element overflows and every element within 2^28 of the
+    // row's largest keeps all its bits; the score multiplier of head h then
+    // carries 2^-e_h.
     uint32_t qf[8][2];
+    int q_exp = 0;                                         // e of head gq
     {
         uint32_t w[16];
-        if (gq < g) {
+        if (gq < R.nrows) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                static_cast<const uint16_t *>(a.q) +
-                ((static_cast<int64_t>(b) * a.num_q_heads + hq0 + gq) * kHeadDim + 32 * tq));
+                static_cast<const uint16_t *>(a.q) + (R.id(a, gq) * kHeadDim + 32 * tq));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 v = __ldg(src + i);
@@ -643,6 +716,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             for (int i = 0; i < 16; ++i)
                 w[i] = 0;
         }
+        float q_mul = 1.f;
+        if constexpr (!kBf16Cache) {
+            uint32_t mx = 0;                               // largest |q| of the row, as bf16 bits
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+            mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            q_exp = row_pow2_exponent(mx);
+            q_mul = __int_as_float((127 + q_exp) << 23);
+        }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
 #pragma unroll
@@ -651,7 +735,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     qf[c][j] = w[2 * c + j];
                 } else {
                     const float2 f = bf16x2_to_f32x2(w[2 * c + j]);
-                    qf[c][j] = f32x2_to_f16x2(f.x, f.y);
+                    qf[c][j] = f32x2_to_f16x2(f.x * q_mul, f.y * q_mul);
                 }
             }
         }
@@ -659,7 +743,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 
     const float kscale = kBf16Cache ? 1.f : a.k_scale[kvh];
     const float vscale = kBf16Cache ? 1.f : a.v_scale[kvh];
-    const float qk_scale = a.qk_scale_log2 * kscale;
+    // score multiplier (log2 domain) of the two query heads 2tq, 2tq + 1
+    // whose scores this lane holds: the softmax scale, the K scale and the
+    // undoing of their q rows' power-of-two scaling
+    float qk_col[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = __shfl_sync(0xFFFFFFFFu, q_exp, 4 * (2 * tq + j));
+        qk_col[j] = a.qk_scale_log2 * kscale * __int_as_float((127 - e) << 23);
+    }
+    // Causal limit of those two rows: query token i sees the positions below
+    // len - n_query + 1 + i (with one query token: all of them), kept as a
+    // count from the split's start, at most one chunk past its end.  Below
+    // full_end every row of the CTA sees every token.
+    const int64_t vis0 = len - a.n_query + 1;
+    int vis_col[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int64_t v = vis0 + (R.row0 + 2 * tq + j) / g - t0;
+        vis_col[j] = static_cast<int>(v < -1 ? -1 : (v > a.split_tokens + kChunkTokens ? a.split_tokens + kChunkTokens : v));
+    }
+    const int64_t full_end = min(t1, vis0 + R.row0 / g);
 
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
@@ -672,10 +776,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     int it = 0;
     for (; it < my_chunks; ++it) {
         const int st = it % T::kStages;
-        if (!mbar_wait_bounded(&my_full[st], (it / T::kStages) & 1, kWaitLimitNs)) {
+        // every lane polls; the warp gives up as one if any lane did
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&my_full[st], (it / T::kStages) & 1, a.copy_wait_ns))) {
             failed = true;
             break;
         }
+        if (it == 0 && warp == 0)
+            KVQ_STAMP(2);
         const uint8_t *ks = ring + st * T::kStageBytes;
         const uint8_t *vs = ks + T::kBytes;
         const int c = warp + it * kWarps;
@@ -696,7 +803,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             __syncwarp();
         }
         const int64_t left = t1 - tok;
-        const int n_valid = left < kChunkTokens ? static_cast<int>(left) : kChunkTokens;
+        const int n_valid = left < kChunkTokens ? static_cast<int>(left) : kChunkTokens;   // V rows
+        int s_valid[2];                                  // tokens of the chunk each score column sees
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            s_valid[j] = min(n_valid, vis_col[j] - c * kChunkTokens);
 
         // The chunk's arithmetic; a full chunk (every token valid, the
         // common case) is compiled without the masking of tail tokens.
@@ -742,8 +853,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int row = mt * 16 + gq + ((i & 2) ? 8 : 0);
-                    float x = sc[mt][i] * qk_scale;
-                    x = (kFull || row < n_valid) ? x : -INFINITY;
+                    float x = sc[mt][i] * qk_col[i & 1];
+                    x = (kFull || row < s_valid[i & 1]) ? x : -INFINITY;
                     sc[mt][i] = x;
                     mx[i & 1] = fmaxf(mx[i & 1], x);
                 }
@@ -850,7 +961,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 }
             }
         };
-        if (n_valid == kChunkTokens)
+        if (tok + kChunkTokens <= full_end)
             chunk(std::true_type{});
         else
             chunk(std::false_type{});
@@ -864,14 +975,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
 
     if (failed) {
-        // drain the copies this warp still has in flight, then leave
+        // Drain the copies this warp still has in flight -- the one it gave
+        // up on and those issued after it -- with the full limit, so none
+        // lands in shared memory after the CTA has moved on.  A drain that
+        // gives up too is reported as bit 1.
         if (lane == 0) {
             atomicOr(&g_device_error, 1u);
             s_failed = 1;
         }
         const int issued = my_chunks < it + T::kStages ? my_chunks : it + T::kStages;
-        for (int j = it + 1; j < issued; ++j)
-            mbar_wait_bounded(&my_full[j % T::kStages], (j / T::kStages) & 1, kWaitLimitNs);
+        bool drained = true;
+        for (int j = it; j < issued; ++j)
+            drained &= mbar_wait_bounded(&my_full[j % T::kStages], (j / T::kStages) & 1, kCopyWaitLimitNs);
+        if (!drained && lane == 0)
+            atomicOr(&g_device_error, 2u);
     }
     if (step_check) {                                      // this thread's tag entries
         cp_async_wait_all();
@@ -886,13 +1003,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             s_stale = 1;
     }
     __syncthreads();
+    KVQ_STAMP(3);
     if (s_stale || s_failed) {                             // a failed check outranks a timeout
         if constexpr (kCluster) {
-            const bool stale = cluster_finish(a, b, kvh, s_stale ? kPartialStale : kPartialInvalid, part, finisher);
+            const bool stale = cluster_finish(a, R, s_stale ? kPartialStale : kPartialInvalid, part, finisher);
             if (split == finisher)
                 finish_here(stale);
         } else
-            drop_split(a, b, kvh, split, nsplit, reinterpret_cast<float *>(smem),
+            drop_split(a, R, split, nsplit, reinterpret_cast<float *>(smem),
                        s_stale ? kLseStale : kLseInvalid);
         return;
     }
@@ -924,7 +1042,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     // per-head merge factors of the four warps, computed once (thread h)
     float *sm_f = sm_l + kWarps * kMaxGroup;                          // [8][kWarps] weights
     float *sm_t = sm_f + kMaxGroup * kWarps;                          // [8] 1 / sum, [8] lse
-    if (threadIdx.x < g) {
+    if (threadIdx.x < R.nrows) {
         const int h = threadIdx.x;
         float mmax = -INFINITY;
 #pragma unroll
@@ -938,18 +1056,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
             sm_f[h * kWarps + w] = f;
             lsum += sm_l[w * kMaxGroup + h] * f;
         }
-        sm_t[h] = vscale / lsum;
-        sm_t[kMaxGroup + h] = mmax + __log2f(lsum);
+        // a row that saw no token of this split (causal limit): weight 0
+        sm_t[h] = lsum > 0.f ? vscale / lsum : 0.f;
+        sm_t[kMaxGroup + h] = lsum > 0.f ? mmax + __log2f(lsum) : -INFINITY;
     }
     __syncthreads();
     for (int d = threadIdx.x; d < kHeadDim; d += kThreads)
-    for (int h = 0; h < g; ++h) {
+    for (int h = 0; h < R.nrows; ++h) {
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
             acc += sm_o[(w * kMaxGroup + h) * kMergeStride + merge_col(d)] * sm_f[h * kWarps + w];
         const float val = acc * sm_t[h];
-        const int64_t bh = static_cast<int64_t>(b) * a.num_q_heads + hq0 + h;
+        const int64_t bh = R.id(a, h);
         if constexpr (kCluster) {
             part[kMaxGroup + h * kHeadDim + d] = val;
             if (d == 0)
@@ -962,15 +1081,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 a.ws_lse[bh * a.max_splits + split] = sm_t[kMaxGroup + h];
         }
     }
+    KVQ_STAMP(4);
     if constexpr (kCluster) {
-        const bool stale = cluster_finish(a, b, kvh, kPartialOk, part, finisher);
+        const bool stale = cluster_finish(a, R, kPartialOk, part, finisher);
         if (split == finisher)
             finish_here(stale);
     } else if (nsplit > 1) {
-        publish_and_combine(a, b, kvh, nsplit, reinterpret_cast<float *>(smem) + kScratchOffset);
+        publish_and_combine(a, R, nsplit, reinterpret_cast<float *>(smem) + kScratchOffset);
     } else if (step_check) {                               // one split: its own verdict
         finish_here(false);
     }
+    KVQ_STAMP(6);
 }
 
 template <bool kBf16, bool kPrecise, bool kCluster>
@@ -1023,8 +1144,8 @@ cudaError_t launch_split(const DecodeArgs &a, const CUtensorMap &k_map, const CU
     e = configure<kBf16, kPrecise, kCluster>(dev);
     if (e != cudaSuccess)
         return e;
-    const dim3 grid(static_cast<unsigned>(a.max_splits), static_cast<unsigned>(a.num_kv_heads),
-                    static_cast<unsigned>(a.batch));
+    const dim3 grid(static_cast<unsigned>(a.max_splits),
+                    static_cast<unsigned>(a.num_kv_heads * a.row_blocks), static_cast<unsigned>(a.batch));
     cudaLaunchAttribute attr[2];
     const cudaLaunchConfig_t cfg = launch_config<kBf16, kPrecise, kCluster>(a, grid, stream, attr);
     e = cudaLaunchKernelEx(&cfg, decode_split_kernel<kBf16, kPrecise, kCluster>, k_map, v_map, a);
@@ -1073,6 +1194,16 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
 {
     if (a.batch == 0)
         return cudaSuccess;
+#ifdef KVQ_PHASE_STAMPS
+    {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_phase_stamps);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(p, 0, sizeof(g_phase_stamps), stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+#endif
     return a.cluster ? launch_variant<true>(a, k_map, v_map, stream)
                      : launch_variant<false>(a, k_map, v_map, stream);
 }
@@ -1130,6 +1261,15 @@ int decode_ctas_per_sm(bool bf16_cache)
     cache[key] = n;
     return n;
 }
+
+#ifdef KVQ_PHASE_STAMPS
+cudaError_t read_decode_stamps(unsigned long long *host, size_t count)
+{
+    const size_t n = count < static_cast<size_t>(kStampCtas * kStampPoints) ? count
+                                                                            : kStampCtas * kStampPoints;
+    return cudaMemcpyFromSymbol(host, g_phase_stamps, n * sizeof(unsigned long long));
+}
+#endif
 
 cudaError_t read_device_error(uint32_t *bits, bool clear)
 {

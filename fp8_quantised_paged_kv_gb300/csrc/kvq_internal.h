@@ -76,11 +76,13 @@ int w4a16_cluster_capacity(int splits);
 cudaError_t read_w4_error(uint32_t *bits, bool clear);
 
 // Workspace layout (bytes from the workspace base):
-//   [0, counter_bytes)       uint32 arrivals[B][Hkv]: splits of each (request, KV
-//                            head) that have published; zero before the first
-//                            call, and every call leaves them zero
-//   [counter_bytes, +lse)    fp32 lse[B][Hq][S]  (log2 domain, NaN = invalid split)
-//   [.., +o)                 fp32 o[B][Hq][S][D]  (each split's normalised output)
+//   [0, counter_bytes)       uint32 arrivals[B][Hkv][row_blocks]: splits of each
+//                            (request, KV head, row block) that have published;
+//                            zero before the first call, and every call leaves
+//                            them zero
+//   [counter_bytes, +lse)    fp32 lse[B][n_query][Hq][S]  (log2 domain, NaN =
+//                            invalid split, -inf = a split that saw no token)
+//   [.., +o)                 fp32 o[B][n_query][Hq][S][D]  (each split's normalised output)
 struct DecodeArgs {
     const void *q;                   // bf16 [B][Hq][D]
     const float *k_scale, *v_scale;  // [Hkv] (unused for bf16 cache)
@@ -100,9 +102,19 @@ struct DecodeArgs {
     const uint32_t *expected_tags;   // in-launch tag check (kvq_decode_step): [B][max_pages],
     const uint32_t *page_tags;       // [num_pages] and the flags written, [B]; else null and
     uint8_t *abort_out;              // abort_flags (if any) is read instead
+    int32_t n_query;                 // new query tokens per request (q, out: [B][n_query][Hq][D])
+    int32_t row_blocks;              // CTAs per (split, request, KV head): ceil(n_query * g / 8)
     float qk_scale_log2;             // softmax_scale * log2(e)
+    uint64_t copy_wait_ns;           // a consumer's limit on one copy wait (0: give up at once)
     bool out_fp32, bf16_cache;
 };
+
+// Default limit of a wait on a bulk copy in the decode kernel: about one
+// second.  The drain that follows a timeout always waits this long.
+constexpr uint64_t kCopyWaitLimitNs = 1000000000ull;
+// The limit decode launches use for a consumer's copy waits: the default
+// unless the diagnostics entry point changed it.
+uint64_t decode_copy_wait_ns();
 
 // Split kernel with the combine fused into its epilogue.  The tensor maps
 // describe the K and V caches as 2-D [rows][128 bytes] tensors with 128-byte
@@ -123,6 +135,13 @@ inline int tma_box_rows(int page_size, bool bf16_cache)
 }
 
 cudaError_t read_device_error(uint32_t *bits, bool clear);
+
+#ifdef KVQ_PHASE_STAMPS
+// Instrumented build only: the %globaltimer stamps of the last decode launch
+// ([CTA][8] points) and of the last tag-check + append launch ([CTA][2]).
+cudaError_t read_decode_stamps(unsigned long long *host, size_t count);
+cudaError_t read_check_stamps(unsigned long long *host, size_t count);
+#endif
 
 // SMs of the current device, queried once per device.  A host with no usable
 // device (the planner's host-only queries) plans for a 152-SM GB300.

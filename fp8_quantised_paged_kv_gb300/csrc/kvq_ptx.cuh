@@ -166,10 +166,12 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 
 // Wait for phase `parity` of the barrier to complete, giving up after about
 // `limit_ns` nanoseconds (and after 2^30 polls in any case).  Returns false
-// on timeout.
+// on timeout.  A limit of 0 gives up at once, without looking.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns)
 {
+    if (limit_ns == 0)
+        return false;
     if (mbar_try_wait(bar, parity))
         return true;
     uint64_t start = global_timer_ns();
@@ -236,6 +238,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

@@ -16,11 +16,27 @@ namespace kvq {
 namespace {
 
 constexpr int kStepThreads = 512;
+
+#ifdef KVQ_PHASE_STAMPS
+// Instrumented build only: %globaltimer at entry (point 0) and exit (1) of
+// thread 0 of every CTA of the last launch.
+constexpr int kCheckStampCtas = 4096;
+__device__ unsigned long long g_check_stamps[kCheckStampCtas * 2];
+__device__ __forceinline__ void check_stamp(int point)
+{
+    if (threadIdx.x == 0 && blockIdx.x < kCheckStampCtas)
+        g_check_stamps[blockIdx.x * 2 + point] = global_timer_ns();
+}
+#define KVQ_CHECK_STAMP(p) check_stamp(p)
+#else
+#define KVQ_CHECK_STAMP(p) ((void)0)
+#endif
 constexpr int kMaxRowsPerPass = kStepThreads / kThreadsPerRow;   // 32 rows (K and V of 16 heads)
 
 template <bool kBf16Cache>
 __global__ void __launch_bounds__(kStepThreads) tag_check_append_kernel(TagCheckArgs t, AppendArgs a)
 {
+    KVQ_CHECK_STAMP(0);
     grid_launch_dependents();              // a dependent decode launch may begin now
     const int64_t r = blockIdx.x;
     const int rows = 2 * a.num_kv_heads;
@@ -42,6 +58,7 @@ __global__ void __launch_bounds__(kStepThreads) tag_check_append_kernel(TagCheck
                                           t.max_pages_per_seq, t.page_size, t.num_pages, r);
     if (threadIdx.x == 0)
         t.abort_flags[r] = bad ? 1 : 0;
+    KVQ_CHECK_STAMP(1);
     if (bad || slot < 0 || slot >= a.num_slots)
         return;
     const int64_t page = slot / a.page_size;
@@ -68,11 +85,29 @@ cudaError_t launch_tag_check_append(const TagCheckArgs &t, const AppendArgs &a, 
 {
     if (t.batch == 0)
         return cudaSuccess;
+#ifdef KVQ_PHASE_STAMPS
+    {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_check_stamps);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(p, 0, sizeof(g_check_stamps), stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+#endif
     if (a.bf16_cache)
         tag_check_append_kernel<true><<<static_cast<unsigned>(t.batch), kStepThreads, 0, stream>>>(t, a);
     else
         tag_check_append_kernel<false><<<static_cast<unsigned>(t.batch), kStepThreads, 0, stream>>>(t, a);
     return cudaGetLastError();
 }
+
+#ifdef KVQ_PHASE_STAMPS
+cudaError_t read_check_stamps(unsigned long long *host, size_t count)
+{
+    const size_t n = count < static_cast<size_t>(kCheckStampCtas * 2) ? count : kCheckStampCtas * 2;
+    return cudaMemcpyFromSymbol(host, g_check_stamps, n * sizeof(unsigned long long));
+}
+#endif
 
 } // namespace kvq

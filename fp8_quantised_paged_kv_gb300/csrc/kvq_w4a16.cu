@@ -213,7 +213,8 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
     int it = 0;
     for (; it < my_blocks; ++it) {
         const int st = it % kW4Stages;
-        if (!mbar_wait_bounded(&my_full[st], (it / kW4Stages) & 1, kW4WaitLimitNs)) {
+        // every lane polls; the warp gives up as one if any lane did
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&my_full[st], (it / kW4Stages) & 1, kW4WaitLimitNs))) {
             failed = true;
             break;
         }
@@ -284,13 +285,18 @@ w4a16_kernel(const __grid_constant__ CUtensorMap w_map, const W4Args a)
         }
     }
     if (failed) {
+        // drain every copy still in flight (the one given up on included)
+        // with the full limit; bit 1 if that gives up too
         if (lane == 0) {
             atomicOr(&g_w4_error, 1u);
             s_failed = 1;
         }
         const int issued = my_blocks < it + kW4Stages ? my_blocks : it + kW4Stages;
-        for (int j = it + 1; j < issued; ++j)
-            mbar_wait_bounded(&my_full[j % kW4Stages], (j / kW4Stages) & 1, kW4WaitLimitNs);
+        bool drained = true;
+        for (int j = it; j < issued; ++j)
+            drained &= mbar_wait_bounded(&my_full[j % kW4Stages], (j / kW4Stages) & 1, kW4WaitLimitNs);
+        if (!drained && lane == 0)
+            atomicOr(&g_w4_error, 2u);
     }
 
     // ---- the four warps' partials (each in its own idle ring), then the CTA's

@@ -230,10 +230,13 @@ KVQ_API kvq_status kvq_decode_plan(const kvq_cache_desc *desc, int32_t batch, in
  *   with K^ = e4m3 value * k_scale[kvh] (bf16 cache: the bf16 value), same
  *   for V.
  *
- *   q              bf16 [B][Hq][D].  On the FP8 path q is used in f16, which
- *                  is exact for |q| in [2^-14, 65504]; smaller magnitudes lose
- *                  relative precision (absolute error < 2^-25) and larger
- *                  ones overflow.
+ *   q              bf16 [B][Hq][D], any finite values.  On the FP8 path the
+ *                  product runs in f16: each q row is first multiplied by the
+ *                  power of two that puts its largest magnitude in [2^14,
+ *                  2^15) (exact) and the score multiplier divides it out, so
+ *                  nothing overflows; an element more than 2^28 times smaller
+ *                  than its row's largest loses low bits (error below 2^-39 of
+ *                  that largest magnitude).
  *   k_cache, v_cache, desc  as in kvq_append.
  *   k_scale, v_scale  fp32 [Hkv] (ignored, may be NULL, for the bf16 cache).
  *   block_table, max_pages_per_seq, seq_lens  as in kvq_tag_check.
@@ -264,6 +267,44 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, in
                            const uint8_t *abort_flags, void *out, int32_t out_dtype,
                            void *workspace, size_t workspace_bytes, int32_t num_splits,
                            kvq_stream_t stream);
+
+/*
+ * kvq_decode_plan_mt / kvq_decode_attn_mt -- decode attention with several
+ * new query tokens per request (verifying speculative drafts).  The source
+ * pages describe one new token per step; this extends kvq_decode_attn's
+ * definition: the n = num_query_tokens new tokens are the request's last n
+ * positions, already in the cache (kvq_append), and query token i attends
+ * causally to positions 0 .. seq_lens[r] - n + i:
+ *   for query token i, query head h of request r (KV head kvh = h / g):
+ *     s_j = softmax_scale * <q[r][i][h], K^_j>,   j = 0 .. seq_lens[r] - n + i
+ *     out[r][i][h] = sum_j exp(s_j - max s) V^_j / sum_j exp(s_j - max s)
+ *
+ *   q              bf16 [B][n][Hq][D] (row r * n + i of a [B * n][Hq][D] array).
+ *   out            [B][n][Hq][D], bf16 or fp32 per out_dtype.  A query with no
+ *                  position to attend to (seq_lens[r] < n - i) gets zeros, as
+ *                  does every query of a request kvq_decode_attn would zero.
+ *   num_query_tokens  n, 1 to 16 (KVQ_ERR_UNSUPPORTED above); n = 1 is
+ *                  kvq_decode_attn.
+ *   Every other argument as in kvq_decode_plan / kvq_decode_attn; the
+ *   workspace size comes from kvq_decode_plan_mt with the same n.
+ * One launch.  A CTA serves up to 8 query rows (token, head) of one (split,
+ * request, KV head); when n * g is larger, ceil(n * g / 8) CTAs stream the
+ * same pages (each reads them; the copies share them through L2).
+ */
+KVQ_API kvq_status kvq_decode_plan_mt(const kvq_cache_desc *desc, int32_t batch,
+                                      int32_t num_query_tokens, int32_t num_q_heads,
+                                      int32_t max_pages_per_seq, int32_t num_splits,
+                                      int32_t *split_tokens, int32_t *max_splits,
+                                      size_t *workspace_bytes);
+KVQ_API kvq_status kvq_decode_attn_mt(const kvq_cache_desc *desc, const void *q, int32_t batch,
+                                      int32_t num_query_tokens, int32_t num_q_heads,
+                                      const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int32_t max_pages_per_seq,
+                                      const int32_t *seq_lens, float softmax_scale,
+                                      const uint8_t *abort_flags, void *out, int32_t out_dtype,
+                                      void *workspace, size_t workspace_bytes, int32_t num_splits,
+                                      kvq_stream_t stream);
 
 /*
  * kvq_decode_attn_append -- kvq_append of each request's new token followed
@@ -359,6 +400,11 @@ KVQ_API kvq_status kvq_w4a16_gemm(const void *x, const uint8_t *w, const void *s
                                   int32_t n, int32_t k, void *y, int32_t out_dtype, int32_t num_splits,
                                   kvq_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Calibration and test hooks.  Not part of the decode path: a deployment
+ * never needs them.
+ * ------------------------------------------------------------------------ */
+
 /*
  * kvq_read_probe -- calibration, not part of the decode path: read `bytes`
  * of device memory at `src` once, with a plain streaming kernel (16-byte
@@ -385,7 +431,9 @@ KVQ_API kvq_status kvq_read_probe(const void *src, size_t bytes, uint32_t *sink,
  *     num_splits, or use kvq_decode_attn with a workspace of your own.
  *   - The first call on a device looks up the array's device address on the
  *     current device (once per device); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process: after
+ *     cudaDeviceReset (or anything else that destroys the device's primary
+ *     context) restart the process before calling this again.
  *   - All calls share the one array and it keeps the last call's contents;
  *     each call clears the part that must start at zero (the arrival
  *     counters) on its stream before the kernel runs.  Calls that overlap on
@@ -404,12 +452,32 @@ KVQ_API kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc *desc, const v
                                              kvq_stream_t stream);
 
 /*
+ * kvq_diag_set_copy_wait_ns -- test hook, process-wide: the time limit the
+ * decode kernel (kvq_decode_attn and every call that runs its kernel) gives a
+ * warp's wait on each of its bulk copies, for launches made after this call.
+ * ns < 0 or above the default restores the default (about one second); 0
+ * makes every warp give up at its first wait, without looking.  Whatever the
+ * setting, a warp that gave up then waits for its copies still in flight
+ * with the default limit, so a shortened limit runs the failure path
+ * (kvq_device_error bit 0, zeros for every (request, KV head) a failed CTA
+ * served) without leaving a copy unaccounted for.  Not thread-safe against
+ * launches on other threads.
+ */
+KVQ_API kvq_status kvq_diag_set_copy_wait_ns(int64_t ns);
+
+/*
  * kvq_device_error -- HOST call, synchronous: reads (into *bits, host
  * memory) and, if `clear` is non-zero, resets the sticky device error word
- * of the current device.  Bit 0: a bulk-copy wait in the decode split kernel
- * gave up after its time limit (about one second); the kernel then drained
- * its copies and returned without writing that CTA's results.  0 means no
- * such event since the last clear.
+ * of the current device.
+ *   Bit 0: a bulk-copy wait in the decode kernel or the INT4 kernel gave up
+ *          after its time limit; the warp then waited for its copies still in
+ *          flight and the CTA returned without its results (the requests it
+ *          served, or the INT4 tile, get zeros).
+ *   Bit 1: that wait for the copies in flight gave up as well, so a copy may
+ *          still land in shared memory that a later CTA uses: results of the
+ *          launches made since are undefined; synchronise the device, check
+ *          the bits and rerun them.
+ * 0 means no such event since the last clear.
  */
 KVQ_API kvq_status kvq_device_error(uint32_t *bits, int32_t clear);
 

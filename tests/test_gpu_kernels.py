@@ -294,6 +294,45 @@ def test_decode_every_e4m3_code_decodes_exactly():
     assert np.array_equal(got[1, 0], dec[126:])
 
 
+def _bf16_bits(x):
+    return W.f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+@pytest.mark.parametrize("cache", ["fp8", "bf16"])
+def test_decode_q_rows_far_outside_the_f16_range(cache):
+    """Any finite bf16 q is valid input.  The FP8 path multiplies each q row by
+    an exact power of two before its f16 product, so rows at 1e6 or 1e30 do
+    not overflow and rows at 1e-6, 1e-30 or bf16 subnormals keep their bits;
+    the outputs match the oracle, which takes q as given."""
+    w = W.make_custom([37, 500, 1000, 2049], group=8, page_size=16, seed=31, outlier_frac=0.01)
+    cd = kvq.KVQ_CACHE_FP8_E4M3 if cache == "fp8" else kvq.KVQ_CACHE_BF16
+    dw = DeviceWorkload(w, cd)
+    dw.append()
+    rng = np.random.default_rng(32)
+    base = rng.standard_normal((w.batch, w.num_q_heads, w.head_dim)).astype(np.float32)
+    mult = np.ones((w.batch, w.num_q_heads, 1), np.float32)
+    mult[0] = 1e6                                  # every head of request 0 far above 65504
+    mult[1] = 1e-6                                 # every head of request 1 far below 2^-14
+    row_mults = [1e6, 1e-6, 1e30, 1e-30, 0.0, 1e-39, 1.0, 3e4]   # one per head of a group
+    for kvh in range(w.num_kv_heads):
+        mult[2, kvh * 8:(kvh + 1) * 8, 0] = row_mults
+    q = base * mult
+    q[2, 6, :4] = 2e5                              # a row of N(0,1) with four elements at 2e5
+    q[3, 1, 5] = -7e4                              # one element just beyond f16 in a normal row
+    q_bits = _bf16_bits(q)
+    dw.q.copy_(torch.from_numpy(q_bits.view(np.int16)).to(DEV).view(torch.bfloat16))
+    kc, vc = oracle_caches(dw)
+    ref = oracle_attention(dw, kc, vc, q=q_bits)
+    assert np.all(np.isfinite(ref))
+    for splits in (0, 1, 12):
+        for fp32 in (True, False):
+            out = dw.out(fp32)
+            dw.attend(out, dw.workspace(splits), None, splits)
+            torch.cuda.synchronize()
+            assert_close(out_to_np(out), ref, "fp32" if fp32 else "bf16",
+                         f"{cache} q rows far from 1, splits {splits}")
+
+
 # ------------------------------------------------- fused tag check + append
 
 @pytest.mark.parametrize("bf16", [False, True])

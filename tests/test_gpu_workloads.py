@@ -97,6 +97,25 @@ def test_long4_sampled_error_vs_length():
     print("long4 max |gpu - oracle| by context length:", errs)
 
 
+def test_long4_at_256_splits_of_4096_tokens():
+    """The long-context workload with its contexts cut into 4,096-token
+    splits: 32, 64, 128 and 256 splits per request, merged by their
+    log-sum-exp weights through the workspace; the shortest and the longest
+    request against the oracle."""
+    w = W.make("long4")
+    dw = DeviceWorkload(w)
+    split_tokens, max_splits, _ = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads,
+                                                      w.max_pages_per_seq, 256)
+    assert (split_tokens, max_splits) == (4096, 256)
+    assert [-(-int(L) // split_tokens) for L in w.seq_lens] == [32, 64, 128, 256]
+    out = dw.out(False)
+    dw.step(out, dw.workspace(256), 256)
+    torch.cuda.synchronize()
+    assert int(dw.abort.sum().item()) == 0
+    for r in (0, 3):
+        _check_request(dw, out, r, "bf16")
+
+
 def test_split_counts_agree_at_full_size():
     dw, out = _step("ragged64", fp32=True)
     for splits in (1, 7):

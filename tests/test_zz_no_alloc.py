@@ -13,7 +13,7 @@ import torch
 
 import fp8_quantised_paged_kv_gb300 as kvq
 import workloads as W
-from gpu_util import assert_close, out_to_np
+from gpu_util import assert_close, oracle_attention, oracle_caches, out_to_np
 from kvq_harness import DeviceWorkload
 
 pytestmark = pytest.mark.gpu
@@ -33,23 +33,33 @@ def _static_call(dw, out, num_splits, abort=None):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("num_splits", [0, 4])
+# 0: the planner's choice; 4: a cluster of 4 splits (partials in shared
+# memory); 12: more splits than a cluster holds, so the partials go through
+# the built-in scratch and the last split to finish merges them
+@pytest.mark.parametrize("num_splits", [0, 4, 12])
 def test_static_scratch_matches_the_workspace_entry_point_twice(num_splits):
     w = W.make_custom([3000, 700, 4100, 1, 2500, 0], group=8, page_size=16, seed=21,
                       outlier_frac=0.01)
     dw = DeviceWorkload(w)
     dw.append()
-    abort = torch.zeros(w.batch, dtype=torch.uint8, device="cuda")
-    abort[2] = 1
+    if num_splits == 12:
+        need = kvq.kvq_decode_plan(dw.desc, w.batch, w.num_q_heads, w.max_pages_per_seq, 12)[2]
+        assert (w.batch * w.num_kv_heads * 4 + 255) // 256 * 256 < need <= (16 << 20)
+    abort_np = np.zeros(w.batch, np.uint8)
+    abort_np[2] = 1
+    abort = torch.from_numpy(abort_np).to("cuda")
     ref = dw.out()
     dw.attend(ref, dw.workspace(num_splits), abort, num_splits)
     torch.cuda.synchronize()
+    kc, vc = oracle_caches(dw)
+    oracle_out = oracle_attention(dw, kc, vc, abort_np)
     for call in range(2):
         out = dw.out()
         out.fill_(7.0)
         assert _static_call(dw, out, num_splits, abort) == 0
         torch.cuda.synchronize()
         assert_close(out_to_np(out), out_to_np(ref), "bf16", f"static scratch, call {call + 1}")
+        assert_close(out_to_np(out), oracle_out, "bf16", f"static scratch vs oracle, call {call + 1}")
     assert kvq.kvq_device_error() == 0
 
 
