@@ -319,6 +319,34 @@ class ChurnGraphStep:
         self.out = [torch.empty(shape_q, dtype=torch.bfloat16, device=d) for _ in range(dev.layers)]
         self.graph = None
 
+    INPUTS = ("bt", "exp", "seq", "tags", "slots")
+
+    def pack_inputs(self):
+        """Re-home every per-step input (tables, tags, slots and each layer's q,
+        new K and new V) in one device buffer of 256-byte-aligned segments,
+        and return it with a pinned host buffer of the same size, so that a
+        step fed from host memory is one host-to-device copy."""
+        torch, dev = self.dev.torch, self.dev
+        tensors = [(n, None) for n in self.INPUTS] + \
+            [(n, l) for n in ("q", "kn", "vn") for l in range(dev.layers)]
+        get = lambda n, l: getattr(self, n) if l is None else getattr(self, n)[l]
+        offs, total = [], 0
+        for n, l in tensors:
+            t = get(n, l)
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.zeros(total, dtype=torch.uint8, device=dev.device)
+        for (n, l), o in zip(tensors, offs):
+            t = get(n, l)
+            view = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            if l is None:
+                setattr(self, n, view)
+            else:
+                getattr(self, n)[l] = view
+        self.packed = buf
+        self.packed_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        return self.packed_host, self.packed
+
     def load(self):
         """Copy this step's tables and per-layer values into the fixed buffers.
         Returns (bt, exp, seq, stale, slots) on the host."""
@@ -337,19 +365,41 @@ class ChurnGraphStep:
             self.vn[l].copy_(vn)
         return bt, exp, seq, stale, slots
 
-    def launch(self, stream=None):
+    def pack_outputs(self):
+        """Every layer's output as a view of one [layers][B][Hq][D] tensor (one
+        device-to-host copy reads them all); returns that tensor."""
+        torch, dev = self.dev.torch, self.dev
+        allout = torch.empty((dev.layers,) + tuple(self.out[0].shape), dtype=self.out[0].dtype,
+                             device=dev.device)
+        self.out = [allout[l] for l in range(dev.layers)]
+        return allout
+
+    def launch(self, stream=None, after_check=None, layer_events=None):
+        """The step's launches: the tag check, then every layer.  Optional
+        CUDA events: `after_check` is recorded between the check and the first
+        layer, layer_events[l] = (start, end) around layer l's decode launch."""
         dev, kvq, s = self.dev, self.dev.kvq, self.dev.s
         kvq.kvq_tag_check(self.bt, self.exp, self.seq, s.ps, self.tags, dev.abort, stream)
+        if after_check is not None:
+            after_check.record(stream)
         for l in range(dev.layers):
+            if layer_events is not None and self.fused_append:
+                layer_events[l][0].record(stream)
             if self.fused_append:
                 kvq.kvq_decode_attn_append(dev.desc, self.q[l], dev.k[l], dev.v[l], dev.k_scale[l],
                                            dev.v_scale[l], self.bt, self.seq, dev.sigma, dev.abort,
                                            self.kn[l], self.vn[l], self.out[l], dev.ws, 0, stream)
+                if layer_events is not None:
+                    layer_events[l][1].record(stream)
                 continue
             kvq.kvq_append(dev.desc, self.kn[l], self.vn[l], self.slots, dev.k_scale[l], dev.v_scale[l],
                            dev.abort, dev.k[l], dev.v[l], stream)
+            if layer_events is not None:
+                layer_events[l][0].record(stream)
             kvq.kvq_decode_attn(dev.desc, self.q[l], dev.k[l], dev.v[l], dev.k_scale[l], dev.v_scale[l],
                                 self.bt, self.seq, dev.sigma, dev.abort, self.out[l], dev.ws, 0, stream)
+            if layer_events is not None:
+                layer_events[l][1].record(stream)
 
     def capture(self):
         """Capture launch() as a CUDA graph (after one eager launch has run
