@@ -244,6 +244,19 @@ def cpu_oracle_step_runner(workload: str, seed: int = 0, requests: int = 1):
     return run, w.kv_bytes(1), oracle.num_threads(), w
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu), or the machine type if unknown."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(workload: str, budget_s: float = 4.0, requests: int = 1):
     """The unchanged oracle, timed on the host cores for about budget_s
     seconds on a sample of the workload (its first `requests` requests, one
@@ -258,7 +271,7 @@ def cpu_baseline(workload: str, budget_s: float = 4.0, requests: int = 1):
             break
     dt = time.perf_counter() - t0
     return {"value": round(kv_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
+            "cpu": host_cpu_model(), "nproc": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} decode steps (tag check, append, attention; one layer) of {w.batch} "
                       f"of the {workload} requests ({w.kv_tokens()} tokens each step) in "
                       f"{dt:.1f} s, fp64 C oracle on the host CPU"}
@@ -296,7 +309,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
         "tokens_per_s": round(w.batch / (ms / 1e3), 3),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                         "kind": "oracle",
+                         "cpu": host_cpu_model(), "nproc": os.cpu_count(), "kind": "oracle",
                          "sample": f"each step = the decode step (tag check, append, attention) "
                                    f"of {w.batch} of the {name} requests in one layer "
                                    f"({w.kv_tokens()} tokens), fp64 C oracle"},
@@ -801,10 +814,11 @@ def run_phase_stamps(args):
     CTA entry, in microseconds."""
     import ctypes
     import torch
+    import importlib
     import fp8_quantised_paged_kv_gb300 as kvq
-    from fp8_quantised_paged_kv_gb300 import build as kbuild
     import workloads as W
     from kvq_harness import DeviceWorkload
+    kbuild = importlib.import_module("fp8_quantised_paged_kv_gb300.build")
     kvq.load(kbuild.build(stamps=True))          # every call of this run goes to the instrumented build
     env = Env(args)
     lib = kvq.load()
@@ -841,7 +855,9 @@ def run_phase_stamps(args):
                 assert lib.kvq_phase_stamps(0, dec.ctypes.data, dec.size) == 0
                 assert lib.kvq_phase_stamps(1, chk.ctypes.data, chk.size) == 0
                 d = dec.reshape(n_cta, 8).astype(np.int64)
-                streamed = d[d[:, 6] > 0]                # CTAs that streamed and finished
+                # nothing is cleared between launches: a CTA that streamed and
+                # finished has an exit stamp later than its entry stamp
+                streamed = d[d[:, 6] >= d[:, 0]]
                 uses_check = form.startswith("two_launch")
                 c = chk.reshape(w.batch, 2).astype(np.int64)
                 t0 = min(int(c[:, 0].min()) if uses_check else 1 << 62, int(d[d[:, 0] > 0, 0].min()))

@@ -130,7 +130,8 @@ int64_t auto_splits(int64_t pairs, int64_t max_ctx, int64_t slots)
 // (16 requests x 8,193 tokens: 3 splits in clusters, 58.5 us, where the
 // multi-wave rule took 7 through the workspace, 79.6 us; 32 x 4,097: one
 // split, 62.0 us against 73.5 us.)
-int64_t single_wave_splits(int64_t pairs, int64_t max_ctx, int64_t unit, int64_t slots, bool bf16)
+int64_t single_wave_splits(int64_t pairs, int64_t max_ctx, int64_t unit, int64_t slots, bool bf16,
+                           bool multi)
 {
     const double bytes_per_tok = bf16 ? 512.0 : 256.0;       // K + V of one token of one KV head
     const double cta_rate = bf16 ? 40e9 : 20e9;               // bytes per second per CTA
@@ -153,7 +154,7 @@ int64_t single_wave_splits(int64_t pairs, int64_t max_ctx, int64_t unit, int64_t
             continue;                                           // the same plan as a smaller n
         last = splits;
         const bool cluster = splits >= 2 && splits <= kvq::kMaxCluster &&
-                             pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16);
+                             pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16, multi);
         if (!cluster && pairs * splits > slots)
             continue;                                           // more than one wave
         const double split_us = static_cast<double>(split) * bytes_per_tok / cta_rate * 1e6;
@@ -168,9 +169,7 @@ int64_t single_wave_splits(int64_t pairs, int64_t max_ctx, int64_t unit, int64_t
     return best;
 }
 
-// Query rows of a CTA (one mma n-tile) and the most new query tokens per
-// request a multi-token call takes.
-constexpr int kRowsPerCta = kvq::kMaxGroup;
+// The most new query tokens per request a multi-token call takes.
 constexpr int kMaxQueryTokens = 16;
 
 kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads,
@@ -193,8 +192,11 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     const int64_t max_ctx = static_cast<int64_t>(max_pages) * d->page_size;
     const int64_t unit = d->page_size > kChunkTokens ? d->page_size : kChunkTokens;
     const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
-    // CTAs per split: one per (request, KV head, block of 8 query rows)
-    const int64_t row_blocks = (static_cast<int64_t>(n_query) * g + kRowsPerCta - 1) / kRowsPerCta;
+    // CTAs per split: one per (request, KV head), or with several query
+    // tokens one per (request, KV head, block of 16 query rows)
+    const bool multi = n_query > 1;
+    const int64_t row_blocks =
+        multi ? (static_cast<int64_t>(n_query) * g + kvq::kMultiRowsPerCta - 1) / kvq::kMultiRowsPerCta : 1;
     const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads * row_blocks;
     p->row_blocks = static_cast<int32_t>(row_blocks);
     if (static_cast<int64_t>(d->num_kv_heads) * row_blocks > 65535)
@@ -204,10 +206,11 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (num_splits > 0) {
         want = num_splits;
     } else {
-        const int64_t slots = static_cast<int64_t>(kvq::device_sm_count()) * kvq::decode_ctas_per_sm(bf16);
+        const int64_t slots =
+            static_cast<int64_t>(kvq::device_sm_count()) * kvq::decode_ctas_per_sm(bf16, multi);
         const int64_t jobs = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads * row_blocks;
         const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
-        want = jobs * big < 4 * slots ? single_wave_splits(jobs, max_ctx, unit, slots, bf16) : 0;
+        want = jobs * big < 4 * slots ? single_wave_splits(jobs, max_ctx, unit, slots, bf16, multi) : 0;
         single_wave = want > 0;
         if (!single_wave)
             want = auto_splits(jobs, max_ctx, slots);
@@ -219,7 +222,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
         // through distributed shared memory, a much shorter tail than the
         // workspace combine; that is worth giving up up to half the splits.
         int64_t c = want < kvq::kMaxCluster ? want : kvq::kMaxCluster;
-        while (c >= 2 && pairs > kvq::decode_cluster_capacity(static_cast<int>(c), bf16))
+        while (c >= 2 && pairs > kvq::decode_cluster_capacity(static_cast<int>(c), bf16, multi))
             --c;
         if (c >= 2 && 2 * c >= want)
             want = c;
@@ -229,7 +232,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (split > kMaxSplitTokens)
         split = kMaxSplitTokens;
     int64_t splits = (max_ctx + split - 1) / split;
-    if (splits > kvq::kMaxSplitsTotal)
+    if (splits > (multi ? kvq::kMultiMaxSplitsPerRequest : kvq::kMaxSplitsTotal))
         return KVQ_ERR_UNSUPPORTED;
     p->split_tokens = static_cast<int32_t>(split);
     p->max_splits = static_cast<int32_t>(splits);
@@ -238,7 +241,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     // the workspace.
     p->cluster = 0;
     if (splits >= 2 && batch > 0 &&
-        pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16))
+        pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16, multi))
         p->cluster = static_cast<int32_t>(splits);
     p->counter_bytes = (static_cast<size_t>(pairs) * 4 + 255) / 256 * 256;
     if (p->counter_bytes == 0)

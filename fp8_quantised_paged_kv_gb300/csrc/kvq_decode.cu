@@ -45,7 +45,9 @@ __device__ unsigned int g_device_error = 0;
 #ifdef KVQ_PHASE_STAMPS
 // Instrumented build only (-DKVQ_PHASE_STAMPS, a library of its own): thread
 // 0 of every CTA of a decode launch records %globaltimer at fixed points;
-// the host clears them before each launch and reads them back.  Points:
+// the host reads them back after the launch (nothing is cleared in between,
+// so no extra operation separates the launch from the one before it: a point
+// a CTA did not reach keeps an older time than its entry).  Points:
 // 0 entry, 1 the programmatic-launch wait returned, 2 warp 0's first chunk
 // landed, 3 every warp done streaming, 4 in-CTA merge done, 5 the combine's
 // first synchronisation passed (cluster barrier or arrival counter),
@@ -148,15 +150,20 @@ __device__ __forceinline__ void store_out(void *out, int64_t idx, float v, bool 
 // The query rows one CTA serves.  The rows of (request b, KV head kvh) are
 // (token i, head h) for the request's n_query new tokens and the g query
 // heads of the group, row i * g + h; a CTA takes rows row0 .. row0 + nrows - 1
-// (at most kMaxGroup: one mma n-tile).  With one query token the rows are
-// the group's heads and one CTA takes them all.
+// (at most rows_per_cta(kMulti)).  With one query token (kMulti false, the
+// kernel compiled for that case) the rows are the group's heads, one mma
+// n-tile of 8, and one CTA takes them all; the multi-token kernel gives each
+// warp two n-tiles (16 rows), so every chunk's conversions serve 16 rows.
+template <bool kMulti>
 struct Rows {
     int b, kvh, row0, nrows;
     int64_t slot;                            // this (request, KV head, row block)'s arrival counter
 
     // Row of q and out ([B][n_query][Hq][D], in units of head_dim) of local row r.
-    __device__ int64_t id(const DecodeArgs &a, int r) const
+    __device__ __forceinline__ int64_t id(const DecodeArgs &a, int r) const
     {
+        if constexpr (!kMulti)
+            return static_cast<int64_t>(b) * a.num_q_heads + kvh * a.group + r;
         const int rr = row0 + r;
         return (static_cast<int64_t>(b) * a.n_query + rr / a.group) * a.num_q_heads + kvh * a.group +
                rr % a.group;
@@ -172,12 +179,29 @@ __device__ __forceinline__ int merge_col(int d) { return d + 2 * (d >> 5); }
 
 // Shared-memory offset (in floats) of the combine scratch: just past the
 // warps' merge area, inside the ring (idle by then).
-constexpr int kScratchOffset =
-    (kWarps * kMaxGroup * kMergeStride + 3 * kWarps * kMaxGroup + 2 * kMaxGroup + 3) / 4 * 4;
-static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kMaxSplitsTotal) * 4 <= Tile<false>::kRingBytes,
+// Query rows of one CTA: one mma n-tile (8) for a single query token, two
+// (16) for the multi-token kernel.
+__host__ __device__ constexpr int rows_per_cta(bool multi) { return multi ? 2 * kMaxGroup : kMaxGroup; }
+
+
+// Shared-memory offset (in floats) of the cluster partial: just past the
+// warps' merge area, inside the ring (idle by then).  The workspace combine's
+// scratch starts at offset 0: it runs after the CTA's own partial has left
+// the merge area for global memory.
+__host__ __device__ constexpr int scratch_offset(bool multi)
+{
+    return (kWarps * rows_per_cta(multi) * kMergeStride + 3 * kWarps * rows_per_cta(multi) +
+            2 * rows_per_cta(multi) + 3) / 4 * 4;
+}
+constexpr int kScratchOffset = scratch_offset(false);
+static_assert((kMaxGroup + kMaxGroup * kMaxSplitsTotal) * 4 <= Tile<false>::kRingBytes,
               "the workspace combine's scratch fits in the idle ring");
+static_assert((2 * kMaxGroup + 2 * kMaxGroup * kMultiMaxSplitsPerRequest) * 4 <= Tile<false>::kRingBytes,
+              "the multi-token workspace combine's scratch fits in the idle ring");
 static_assert((kScratchOffset + kMaxGroup + kMaxGroup * kHeadDim) * 4 <= Tile<false>::kRingBytes,
               "the cluster combine's partial fits in the idle ring");
+static_assert((scratch_offset(true) + 2 * kMaxGroup + 2 * kMaxGroup * kHeadDim) * 4 <= Tile<false>::kRingBytes,
+              "the multi-token cluster partial fits in the idle ring");
 
 // Count this split's arrival for (request b, KV head kvh).  The last split
 // to arrive merges the partials of all nsplit splits of the group:
@@ -215,7 +239,8 @@ __device__ void finish_step(const DecodeArgs &a, int b, int kvh, bool stale)
     }
 }
 
-__device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nsplit, float *scratch)
+template <bool kMulti>
+__device__ void publish_and_combine(const DecodeArgs &a, const Rows<kMulti> &R, int nsplit, float *scratch)
 {
     __shared__ int s_last;
     // The block barrier orders every thread's partial before thread 0's
@@ -230,9 +255,10 @@ __device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nspl
     KVQ_STAMP(5);
     if (!s_last)
         return;
+    constexpr int kRowsT = rows_per_cta(kMulti);
     const int g = R.nrows, n = nsplit;
-    float *s_tot = scratch;                  // [8] sum of weights (0: drop the row)
-    float *s_w = scratch + kMaxGroup;        // [g][n]: lse, then weights
+    float *s_tot = scratch;                  // [kRowsT] sum of weights (0: drop the row)
+    float *s_w = scratch + kRowsT;           // [g][n]: lse, then weights
     for (int i = threadIdx.x; i < g * n; i += kThreads)
         s_w[i] = __ldcg(a.ws_lse + R.id(a, i / n) * a.max_splits + i % n);
     __syncthreads();
@@ -261,18 +287,25 @@ __device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nspl
             s_tot[h] = bad ? 0.f : sum;
     }
     __syncthreads();
-    // thread t: the (head, 4 dims) pairs t and t + 128 of the group's 8 x 32;
-    // eight splits per round, every 16-byte load of a round issued before any
-    // is used, so a round costs one trip to L2
-    constexpr int kRound = 8;
-    static_assert(kMaxGroup * (kHeadDim / 4) == 2 * kThreads, "two (head, 4 dims) pairs per thread");
-    const int hp[2] = {static_cast<int>(threadIdx.x) / 32, static_cast<int>(threadIdx.x + kThreads) / 32};
-    const int cp = 4 * (threadIdx.x % 32);
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-    for (int s0 = 0; s0 < n; s0 += kRound) {
-        float4 v[2][kRound];
+    // thread t: the (row, 4 dims) pairs t, t + 128, ... of the rows x 32;
+    // kRound splits per round, every 16-byte load of a round issued before
+    // any is used, so a round costs one trip to L2
+    constexpr int kPairs = kRowsT * (kHeadDim / 4) / kThreads;          // 2, or 4 with 16 rows
+    constexpr int kRound = kMulti ? 4 : 8;
+    static_assert(kRowsT * (kHeadDim / 4) == kPairs * kThreads, "whole (row, 4 dims) pairs per thread");
+    int hp[kPairs];
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+    for (int q = 0; q < kPairs; ++q)
+        hp[q] = static_cast<int>(threadIdx.x + q * kThreads) / 32;
+    const int cp = 4 * (threadIdx.x % 32);
+    float4 acc[kPairs];
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q)
+        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n; s0 += kRound) {
+        float4 v[kPairs][kRound];
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q)
 #pragma unroll
             for (int j = 0; j < kRound; ++j)
                 v[q][j] = (hp[q] < g && s0 + j < n)
@@ -280,7 +313,7 @@ __device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nspl
                                     a.ws_o + (R.id(a, hp[q]) * a.max_splits + s0 + j) * kHeadDim + cp))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < kPairs; ++q)
 #pragma unroll
             for (int j = 0; j < kRound; ++j)
                 if (hp[q] < g && s0 + j < n) {
@@ -292,7 +325,7 @@ __device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nspl
                 }
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int q = 0; q < kPairs; ++q)
         if (hp[q] < g) {
             const int64_t o0 = R.id(a, hp[q]) * kHeadDim + cp;
             store_out(a.out, o0, s_tot[hp[q]] > 0.f ? acc[q].x / s_tot[hp[q]] : 0.f, a.out_fp32);
@@ -318,7 +351,8 @@ __device__ void publish_and_combine(const DecodeArgs &a, const Rows &R, int nspl
 // A split that cannot produce a result (invalid page id, or a copy that
 // timed out): a single-split request gets zeros; otherwise the split
 // publishes an invalid (NaN) lse so the combine zeroes the request.
-__device__ void drop_split(const DecodeArgs &a, const Rows &R, int split, int nsplit, float *smem,
+template <bool kMulti>
+__device__ void drop_split(const DecodeArgs &a, const Rows<kMulti> &R, int split, int nsplit, float *smem,
                            uint32_t lse_bits = kLseInvalid)
 {
     if (nsplit == 1) {
@@ -330,7 +364,7 @@ __device__ void drop_split(const DecodeArgs &a, const Rows &R, int split, int ns
     }
     if (threadIdx.x < R.nrows)
         a.ws_lse[R.id(a, threadIdx.x) * a.max_splits + split] = __uint_as_float(lse_bits);
-    publish_and_combine(a, R, nsplit, smem + kScratchOffset);
+    publish_and_combine(a, R, nsplit, kMulti ? smem : smem + kScratchOffset);
 }
 
 // What a split contributes to the cluster form of the combine.
@@ -339,7 +373,8 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPa
 // Cluster form of the combine, used when the splits of each (request, KV
 // head) are the CTAs of one thread-block cluster (every split resident at
 // once).  Each CTA leaves its partial in its own shared memory at `part`:
-// [kMaxGroup] lse (log2 domain), then [kMaxGroup][128] normalised o; an empty
+// [rows] lse (log2 domain), then [rows][128] normalised o (rows =
+// rows_per_cta(kMulti)); an empty
 // split (no tokens) publishes lse = -inf (weight 0), an invalid one NaN (its
 // heads get zeros).  After a cluster barrier CTA r merges the query heads
 // h = r, r + n, ... of the group from every peer's partial, read through
@@ -350,11 +385,13 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPa
 // same `finisher`: for kvq_decode_step the rank that reads every peer's
 // verdict, else -1.  Returns, on the finisher, whether any split of the
 // request failed its tag check (false elsewhere).
-__device__ bool cluster_finish(const DecodeArgs &a, const Rows &R, PartialStatus status, float *part,
+template <bool kMulti>
+__device__ bool cluster_finish(const DecodeArgs &a, const Rows<kMulti> &R, PartialStatus status, float *part,
                                int finisher)
 {
     __shared__ int s_any_stale;
-    if (status != kPartialOk && threadIdx.x < kMaxGroup)
+    constexpr int kRowsT = rows_per_cta(kMulti);
+    if (status != kPartialOk && threadIdx.x < kRowsT)
         part[threadIdx.x] = status == kPartialEmpty ? -INFINITY
                             : __uint_as_float(status == kPartialStale ? kLseStale : kLseInvalid);
     cluster_sync();
@@ -385,7 +422,7 @@ __device__ bool cluster_finish(const DecodeArgs &a, const Rows &R, PartialStatus
             if (s < n) {
                 const uint32_t peer = map_shared_rank(base, static_cast<uint32_t>(s));
                 lse[s] = ld_shared_cluster_f32(peer + 4u * h);
-                ov[s] = ld_shared_cluster_v4(peer + 4u * (kMaxGroup + h * kHeadDim + d));
+                ov[s] = ld_shared_cluster_v4(peer + 4u * (kRowsT + h * kHeadDim + d));
             }
         }
         float m = -INFINITY;
@@ -419,8 +456,8 @@ __device__ bool cluster_finish(const DecodeArgs &a, const Rows &R, PartialStatus
     return rank == finisher && s_any_stale != 0;
 }
 
-template <bool kBf16Cache, bool kPreciseP, bool kCluster>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <bool kBf16Cache, bool kPreciseP, bool kCluster, bool kMulti>
+__global__ void __launch_bounds__(kThreads, kMulti ? 2 : kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a)
 {
@@ -438,16 +475,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     __shared__ int s_stale;                                // kvq_decode_step: a page of this split failed
 
     const int split = blockIdx.x, b = blockIdx.z;
-    const int kvh = static_cast<int>(blockIdx.y) / a.row_blocks;
-    const int rb = static_cast<int>(blockIdx.y) % a.row_blocks;   // block of 8 query rows
+    // with several query tokens, blockIdx.y = KV head x row blocks of 8 rows
+    const int kvh = kMulti ? static_cast<int>(blockIdx.y) / a.row_blocks : static_cast<int>(blockIdx.y);
+    const int rb = kMulti ? static_cast<int>(blockIdx.y) % a.row_blocks : 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gq = lane >> 2, tq = lane & 3;
     const int g = a.group, ps = a.page_size;
-    Rows R;
+    Rows<kMulti> R;
     R.b = b;
     R.kvh = kvh;
-    R.row0 = rb * kMaxGroup;
-    R.nrows = min(kMaxGroup, a.n_query * g - R.row0);
+    R.row0 = rb * rows_per_cta(kMulti);
+    R.nrows = kMulti ? min(rows_per_cta(true), a.n_query * g - R.row0) : g;
     R.slot = static_cast<int64_t>(b) * gridDim.y + blockIdx.y;
 
     const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
@@ -512,7 +550,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     if (reporter && zero_request)                          // the check's verdict without a look:
         a.abort_out[b] = len > cap ? 1 : 0;                // too long fails, empty passes
     const int nsplit = zero_request ? 1 : static_cast<int>((len + a.split_tokens - 1) / a.split_tokens);
-    float *part = reinterpret_cast<float *>(smem) + kScratchOffset;   // cluster partial
+    float *part = reinterpret_cast<float *>(smem) + scratch_offset(kMulti);   // cluster partial
     // kvq_decode_step: the split that finishes the step of a request with
     // tokens in the cluster form and when there is one split -- the last
     // split, which holds the new token (the workspace form's combine
@@ -638,7 +676,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int parts = kChunkTokens / box_tok;                       // 1 or 2 copies per tensor
     const uint32_t part_bytes = static_cast<uint32_t>(box_tok * T::kRowBytes);
     // evict-first unless other row blocks of the split read the same pages
-    const uint64_t policy = a.row_blocks > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
+    const uint64_t policy = kMulti && a.row_blocks > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
 
 
     // Issue the copies of this warp's local chunk `it` (lane 0 only).
@@ -699,13 +737,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     // changes), so no element overflows and every element within 2^28 of the
     // row's largest keeps all its bits; the score multiplier of head h then
     // carries 2^-e_h.
-    uint32_t qf[8][2];
-    int q_exp = 0;                                         // e of head gq
-    {
+    constexpr int kNT = rows_per_cta(kMulti) / kMaxGroup;   // mma n-tiles of query rows per warp
+    constexpr int kRowsT = rows_per_cta(kMulti);
+    uint32_t qf[kNT][8][2];
+    int q_exp[kNT];                                        // e of row nt * 8 + gq
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        q_exp[nt] = 0;
         uint32_t w[16];
-        if (gq < R.nrows) {
+        if (nt * kMaxGroup + gq < R.nrows) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                static_cast<const uint16_t *>(a.q) + (R.id(a, gq) * kHeadDim + 32 * tq));
+                static_cast<const uint16_t *>(a.q) + (R.id(a, nt * kMaxGroup + gq) * kHeadDim + 32 * tq));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 v = __ldg(src + i);
@@ -724,18 +766,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
             mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
             mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            q_exp = row_pow2_exponent(mx);
-            q_mul = __int_as_float((127 + q_exp) << 23);
+            q_exp[nt] = row_pow2_exponent(mx);
+            q_mul = __int_as_float((127 + q_exp[nt]) << 23);
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 if constexpr (kBf16Cache) {
-                    qf[c][j] = w[2 * c + j];
+                    qf[nt][c][j] = w[2 * c + j];
                 } else {
                     const float2 f = bf16x2_to_f32x2(w[2 * c + j]);
-                    qf[c][j] = f32x2_to_f16x2(f.x * q_mul, f.y * q_mul);
+                    qf[nt][c][j] = f32x2_to_f16x2(f.x * q_mul, f.y * q_mul);
                 }
             }
         }
@@ -746,31 +788,43 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     // score multiplier (log2 domain) of the two query heads 2tq, 2tq + 1
     // whose scores this lane holds: the softmax scale, the K scale and the
     // undoing of their q rows' power-of-two scaling
-    float qk_col[2];
+    float qk_col[kNT][2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int e = __shfl_sync(0xFFFFFFFFu, q_exp, 4 * (2 * tq + j));
-        qk_col[j] = a.qk_scale_log2 * kscale * __int_as_float((127 - e) << 23);
-    }
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int e = __shfl_sync(0xFFFFFFFFu, q_exp[nt], 4 * (2 * tq + j));
+            qk_col[nt][j] = a.qk_scale_log2 * kscale * __int_as_float((127 - e) << 23);
+        }
     // Causal limit of those two rows: query token i sees the positions below
     // len - n_query + 1 + i (with one query token: all of them), kept as a
     // count from the split's start, at most one chunk past its end.  Below
     // full_end every row of the CTA sees every token.
-    const int64_t vis0 = len - a.n_query + 1;
-    int vis_col[2];
+    [[maybe_unused]] int vis_col[kNT][2] = {};
+    int64_t full_end = t1;
+    if constexpr (kMulti) {
+        const int64_t vis0 = len - a.n_query + 1;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int64_t v = vis0 + (R.row0 + 2 * tq + j) / g - t0;
-        vis_col[j] = static_cast<int>(v < -1 ? -1 : (v > a.split_tokens + kChunkTokens ? a.split_tokens + kChunkTokens : v));
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int64_t v = vis0 + (R.row0 + nt * kMaxGroup + 2 * tq + j) / g - t0;
+                vis_col[nt][j] = static_cast<int>(
+                    v < -1 ? -1 : (v > a.split_tokens + kChunkTokens ? a.split_tokens + kChunkTokens : v));
+            }
+        full_end = min(t1, vis0 + R.row0 / g);
     }
-    const int64_t full_end = min(t1, vis0 + R.row0 / g);
 
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
-    float o[8][4];
+    float m_run[kNT][2], l_run[kNT][2];
+    float o[kNT][8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int nt = 0; nt < kNT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+    }
 
     bool failed = false;
     int it = 0;
@@ -804,20 +858,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         }
         const int64_t left = t1 - tok;
         const int n_valid = left < kChunkTokens ? static_cast<int>(left) : kChunkTokens;   // V rows
-        int s_valid[2];                                  // tokens of the chunk each score column sees
+        int s_valid[kNT][2];                             // tokens of the chunk each score column sees
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-            s_valid[j] = min(n_valid, vis_col[j] - c * kChunkTokens);
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                s_valid[nt][j] = kMulti ? min(n_valid, vis_col[nt][j] - c * kChunkTokens) : n_valid;
 
         // The chunk's arithmetic; a full chunk (every token valid, the
         // common case) is compiled without the masking of tail tokens.
         auto chunk = [&](auto full) {
             constexpr bool kFull = decltype(full)::value;
-            // ---- S^T = K Q^T for the two 16-token m-tiles
-            float sc[2][4];
+            // ---- S^T = K Q^T for the two 16-token m-tiles; each K fragment,
+            // converted once, feeds every n-tile of query rows
+            float sc[kNT][2][4];
     #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    #pragma unroll
+                for (int nt = 0; nt < kNT; ++nt)
+                    sc[nt][mt][0] = sc[nt][mt][1] = sc[nt][mt][2] = sc[nt][mt][3] = 0.f;
                 const int r0 = mt * 16 + gq, r1 = r0 + 8;
                 if constexpr (kBf16Cache) {
                     uint32_t w0[16], w1[16];
@@ -831,86 +890,102 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     }
     #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(sc[mt], w0[2 * kk], w1[2 * kk], w0[2 * kk + 1], w1[2 * kk + 1],
-                                 qf[kk][0], qf[kk][1]);
+    #pragma unroll
+                        for (int nt = 0; nt < kNT; ++nt)
+                            mma_bf16(sc[nt][mt], w0[2 * kk], w1[2 * kk], w0[2 * kk + 1], w1[2 * kk + 1],
+                                     qf[nt][kk][0], qf[nt][kk][1]);
                 } else {
                     const uint4 x0a = lds128(ks, swz(r0, 2 * tq)), x0b = lds128(ks, swz(r0, 2 * tq + 1));
                     const uint4 x1a = lds128(ks, swz(r1, 2 * tq)), x1b = lds128(ks, swz(r1, 2 * tq + 1));
                     const uint32_t w0[8] = {x0a.x, x0a.y, x0a.z, x0a.w, x0b.x, x0b.y, x0b.z, x0b.w};
                     const uint32_t w1[8] = {x1a.x, x1a.y, x1a.z, x1a.w, x1b.x, x1b.y, x1b.z, x1b.w};
     #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16(sc[mt], lo16_e4m3x2_to_f16x2(w0[kk]), lo16_e4m3x2_to_f16x2(w1[kk]),
-                                hi16_e4m3x2_to_f16x2(w0[kk]), hi16_e4m3x2_to_f16x2(w1[kk]),
-                                qf[kk][0], qf[kk][1]);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t k0 = lo16_e4m3x2_to_f16x2(w0[kk]), k1 = lo16_e4m3x2_to_f16x2(w1[kk]);
+                        const uint32_t k2 = hi16_e4m3x2_to_f16x2(w0[kk]), k3 = hi16_e4m3x2_to_f16x2(w1[kk]);
+    #pragma unroll
+                        for (int nt = 0; nt < kNT; ++nt)
+                            mma_f16(sc[nt][mt], k0, k1, k2, k3, qf[nt][kk][0], qf[nt][kk][1]);
+                    }
                 }
             }
 
-            // ---- online softmax (log2 domain); lane holds heads 2tq, 2tq+1
-            float mx[2] = {-INFINITY, -INFINITY};
+            // ---- online softmax (log2 domain); lane holds rows nt*8 + 2tq, +1
+            float alpha[kNT][2];
     #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int nt = 0; nt < kNT; ++nt) {
+                float mx[2] = {-INFINITY, -INFINITY};
     #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = mt * 16 + gq + ((i & 2) ? 8 : 0);
-                    float x = sc[mt][i] * qk_col[i & 1];
-                    x = (kFull || row < s_valid[i & 1]) ? x : -INFINITY;
-                    sc[mt][i] = x;
-                    mx[i & 1] = fmaxf(mx[i & 1], x);
+                for (int mt = 0; mt < 2; ++mt) {
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = mt * 16 + gq + ((i & 2) ? 8 : 0);
+                        float x = sc[nt][mt][i] * qk_col[nt][i & 1];
+                        x = (kFull || row < s_valid[nt][i & 1]) ? x : -INFINITY;
+                        sc[nt][mt][i] = x;
+                        mx[i & 1] = fmaxf(mx[i & 1], x);
+                    }
                 }
-            }
-            float alpha[2], base[2];
+                float base[2];
     #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float mnew = fmaxf(m_run[j], warp_max_over_rows(mx[j]));
-                base[j] = mnew == -INFINITY ? 0.f : mnew;
-                alpha[j] = fast_exp2(m_run[j] - base[j]);
-                m_run[j] = mnew;
-            }
-            float psum[2] = {0.f, 0.f};
-    #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-    #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float p = fast_exp2(sc[mt][i] - base[i & 1]);
-                    sc[mt][i] = p;
-                    psum[i & 1] += p;
+                for (int j = 0; j < 2; ++j) {
+                    const float mnew = fmaxf(m_run[nt][j], warp_max_over_rows(mx[j]));
+                    base[j] = mnew == -INFINITY ? 0.f : mnew;
+                    alpha[nt][j] = fast_exp2(m_run[nt][j] - base[j]);
+                    m_run[nt][j] = mnew;
                 }
-            }
+                float psum[2] = {0.f, 0.f};
     #pragma unroll
-            for (int j = 0; j < 2; ++j)
-                l_run[j] = l_run[j] * alpha[j] + psum[j];
+                for (int mt = 0; mt < 2; ++mt) {
     #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                o[i][0] *= alpha[0];
-                o[i][1] *= alpha[1];
-                o[i][2] *= alpha[0];
-                o[i][3] *= alpha[1];
+                    for (int i = 0; i < 4; ++i) {
+                        const float p = fast_exp2(sc[nt][mt][i] - base[i & 1]);
+                        sc[nt][mt][i] = p;
+                        psum[i & 1] += p;
+                    }
+                }
+    #pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + psum[j];
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[nt][i][0] *= alpha[nt][0];
+                    o[nt][i][1] *= alpha[nt][1];
+                    o[nt][i][2] *= alpha[nt][0];
+                    o[nt][i][3] *= alpha[nt][1];
+                }
             }
 
-            // ---- O^T += V^T P^T
+            // ---- O^T += V^T P^T; each V fragment, converted once, feeds
+            // every n-tile
     #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                uint32_t x0, x1;
-                if constexpr (kBf16Cache) {
-                    x0 = f32x2_to_bf16x2(sc[mt][0], sc[mt][1]);
-                    x1 = f32x2_to_bf16x2(sc[mt][2], sc[mt][3]);
-                } else {
-                    x0 = f32x2_to_f16x2(sc[mt][0], sc[mt][1]);
-                    x1 = f32x2_to_f16x2(sc[mt][2], sc[mt][3]);
-                }
-                const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
-                [[maybe_unused]] uint32_t pl0 = 0, pl1 = 0;
-                if constexpr (kPreciseP) {
-                    // second term carries what the 16-bit rounding of P dropped
-                    const float2 h0 = kBf16Cache ? bf16x2_to_f32x2(x0) : f16x2_to_f32x2(x0);
-                    const float2 h1 = kBf16Cache ? bf16x2_to_f32x2(x1) : f16x2_to_f32x2(x1);
-                    const uint32_t y0 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y)
-                                                   : f32x2_to_f16x2(sc[mt][0] - h0.x, sc[mt][1] - h0.y);
-                    const uint32_t y1 = kBf16Cache ? f32x2_to_bf16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y)
-                                                   : f32x2_to_f16x2(sc[mt][2] - h1.x, sc[mt][3] - h1.y);
-                    pl0 = movmatrix_trans(y0);
-                    pl1 = movmatrix_trans(y1);
+                uint32_t pb0[kNT], pb1[kNT];
+                [[maybe_unused]] uint32_t pl0[kNT], pl1[kNT];
+    #pragma unroll
+                for (int nt = 0; nt < kNT; ++nt) {
+                    uint32_t x0, x1;
+                    if constexpr (kBf16Cache) {
+                        x0 = f32x2_to_bf16x2(sc[nt][mt][0], sc[nt][mt][1]);
+                        x1 = f32x2_to_bf16x2(sc[nt][mt][2], sc[nt][mt][3]);
+                    } else {
+                        x0 = f32x2_to_f16x2(sc[nt][mt][0], sc[nt][mt][1]);
+                        x1 = f32x2_to_f16x2(sc[nt][mt][2], sc[nt][mt][3]);
+                    }
+                    pb0[nt] = movmatrix_trans(x0);
+                    pb1[nt] = movmatrix_trans(x1);
+                    if constexpr (kPreciseP) {
+                        // second term carries what the 16-bit rounding of P dropped
+                        const float2 h0 = kBf16Cache ? bf16x2_to_f32x2(x0) : f16x2_to_f32x2(x0);
+                        const float2 h1 = kBf16Cache ? bf16x2_to_f32x2(x1) : f16x2_to_f32x2(x1);
+                        const float *p = sc[nt][mt];
+                        const uint32_t y0 = kBf16Cache ? f32x2_to_bf16x2(p[0] - h0.x, p[1] - h0.y)
+                                                       : f32x2_to_f16x2(p[0] - h0.x, p[1] - h0.y);
+                        const uint32_t y1 = kBf16Cache ? f32x2_to_bf16x2(p[2] - h1.x, p[3] - h1.y)
+                                                       : f32x2_to_f16x2(p[2] - h1.x, p[3] - h1.y);
+                        pl0[nt] = movmatrix_trans(y0);
+                        pl1[nt] = movmatrix_trans(y1);
+                    }
                 }
                 // V rows of token slots 2tq, 2tq+1, 2tq+8, 2tq+9 of this m-tile
                 const int rv = mt * 16 + 2 * tq;
@@ -934,9 +1009,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                         const uint32_t a1 = prmt(R[0][i], R[1][i], 0x7632);
                         const uint32_t a2 = prmt(R[2][i], R[3][i], 0x5410);
                         const uint32_t a3 = prmt(R[2][i], R[3][i], 0x7632);
-                        mma_bf16(o[i], a0, a1, a2, a3, pb0, pb1);
-                        if constexpr (kPreciseP)
-                            mma_bf16(o[i], a0, a1, a2, a3, pl0, pl1);
+    #pragma unroll
+                        for (int nt = 0; nt < kNT; ++nt) {
+                            mma_bf16(o[nt][i], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+                            if constexpr (kPreciseP)
+                                mma_bf16(o[nt][i], a0, a1, a2, a3, pl0[nt], pl1[nt]);
+                        }
                     }
                 } else {
                     uint32_t R[4][4];
@@ -954,9 +1032,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                         const uint32_t p23 = prmt(R[2][i >> 1], R[3][i >> 1], sel);
                         const uint32_t a0 = lo16_e4m3x2_to_f16x2(p01), a1 = hi16_e4m3x2_to_f16x2(p01);
                         const uint32_t a2 = lo16_e4m3x2_to_f16x2(p23), a3 = hi16_e4m3x2_to_f16x2(p23);
-                        mma_f16(o[i], a0, a1, a2, a3, pb0, pb1);
-                        if constexpr (kPreciseP)
-                            mma_f16(o[i], a0, a1, a2, a3, pl0, pl1);
+    #pragma unroll
+                        for (int nt = 0; nt < kNT; ++nt) {
+                            mma_f16(o[nt][i], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+                            if constexpr (kPreciseP)
+                                mma_f16(o[nt][i], a0, a1, a2, a3, pl0[nt], pl1[nt]);
+                        }
                     }
                 }
             }
@@ -1016,49 +1097,56 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
 
     // ---- merge the four warps' states in shared memory (ring is free now)
-    float *sm_o = reinterpret_cast<float *>(smem);                     // [kWarps][8][128]
-    float *sm_m = sm_o + kWarps * kMaxGroup * kMergeStride;           // [kWarps][8]
-    float *sm_l = sm_m + kWarps * kMaxGroup;                          // [kWarps][8]
+    float *sm_o = reinterpret_cast<float *>(smem);                     // [kWarps][kRowsT][128]
+    float *sm_m = sm_o + kWarps * kRowsT * kMergeStride;              // [kWarps][kRowsT]
+    float *sm_l = sm_m + kWarps * kRowsT;                             // [kWarps][kRowsT]
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-        l_run[j] = warp_sum_over_rows(l_run[j]);
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            l_run[nt][j] = warp_sum_over_rows(l_run[nt][j]);
     {
-        float *ow = sm_o + warp * kMaxGroup * kMergeStride;
+        float *ow = sm_o + warp * kRowsT * kMergeStride;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = merge_col(16 * gq + 2 * i);
-            *reinterpret_cast<float2 *>(ow + (2 * tq) * kMergeStride + c) = make_float2(o[i][0], o[i][2]);
-            *reinterpret_cast<float2 *>(ow + (2 * tq + 1) * kMergeStride + c) = make_float2(o[i][1], o[i][3]);
-        }
-        if (gq == 0) {
-            sm_m[warp * kMaxGroup + 2 * tq] = m_run[0];
-            sm_m[warp * kMaxGroup + 2 * tq + 1] = m_run[1];
-            sm_l[warp * kMaxGroup + 2 * tq] = l_run[0];
-            sm_l[warp * kMaxGroup + 2 * tq + 1] = l_run[1];
+        for (int nt = 0; nt < kNT; ++nt) {
+            const int r = nt * kMaxGroup + 2 * tq;                  // rows r, r + 1 of this lane
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = merge_col(16 * gq + 2 * i);
+                *reinterpret_cast<float2 *>(ow + r * kMergeStride + c) = make_float2(o[nt][i][0], o[nt][i][2]);
+                *reinterpret_cast<float2 *>(ow + (r + 1) * kMergeStride + c) =
+                    make_float2(o[nt][i][1], o[nt][i][3]);
+            }
+            if (gq == 0) {
+                sm_m[warp * kRowsT + r] = m_run[nt][0];
+                sm_m[warp * kRowsT + r + 1] = m_run[nt][1];
+                sm_l[warp * kRowsT + r] = l_run[nt][0];
+                sm_l[warp * kRowsT + r + 1] = l_run[nt][1];
+            }
         }
     }
     __syncthreads();
 
-    // per-head merge factors of the four warps, computed once (thread h)
-    float *sm_f = sm_l + kWarps * kMaxGroup;                          // [8][kWarps] weights
-    float *sm_t = sm_f + kMaxGroup * kWarps;                          // [8] 1 / sum, [8] lse
+    // per-row merge factors of the four warps, computed once (thread h)
+    float *sm_f = sm_l + kWarps * kRowsT;                             // [kRowsT][kWarps] weights
+    float *sm_t = sm_f + kRowsT * kWarps;                             // [kRowsT] 1 / sum, [kRowsT] lse
     if (threadIdx.x < R.nrows) {
         const int h = threadIdx.x;
         float mmax = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
-            mmax = fmaxf(mmax, sm_m[w * kMaxGroup + h]);
+            mmax = fmaxf(mmax, sm_m[w * kRowsT + h]);
         float lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float mw = sm_m[w * kMaxGroup + h];
+            const float mw = sm_m[w * kRowsT + h];
             const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - mmax);
             sm_f[h * kWarps + w] = f;
-            lsum += sm_l[w * kMaxGroup + h] * f;
+            lsum += sm_l[w * kRowsT + h] * f;
         }
         // a row that saw no token of this split (causal limit): weight 0
         sm_t[h] = lsum > 0.f ? vscale / lsum : 0.f;
-        sm_t[kMaxGroup + h] = lsum > 0.f ? mmax + __log2f(lsum) : -INFINITY;
+        sm_t[kRowsT + h] = lsum > 0.f ? mmax + __log2f(lsum) : -INFINITY;
     }
     __syncthreads();
     for (int d = threadIdx.x; d < kHeadDim; d += kThreads)
@@ -1066,19 +1154,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
-            acc += sm_o[(w * kMaxGroup + h) * kMergeStride + merge_col(d)] * sm_f[h * kWarps + w];
+            acc += sm_o[(w * kRowsT + h) * kMergeStride + merge_col(d)] * sm_f[h * kWarps + w];
         const float val = acc * sm_t[h];
         const int64_t bh = R.id(a, h);
         if constexpr (kCluster) {
-            part[kMaxGroup + h * kHeadDim + d] = val;
+            part[kRowsT + h * kHeadDim + d] = val;
             if (d == 0)
-                part[h] = sm_t[kMaxGroup + h];
+                part[h] = sm_t[kRowsT + h];
         } else if (nsplit == 1) {
             store_out(a.out, bh * kHeadDim + d, val, a.out_fp32);
         } else {
             a.ws_o[(bh * a.max_splits + split) * kHeadDim + d] = val;
             if (d == 0)
-                a.ws_lse[bh * a.max_splits + split] = sm_t[kMaxGroup + h];
+                a.ws_lse[bh * a.max_splits + split] = sm_t[kRowsT + h];
         }
     }
     KVQ_STAMP(4);
@@ -1087,20 +1175,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         if (split == finisher)
             finish_here(stale);
     } else if (nsplit > 1) {
-        publish_and_combine(a, R, nsplit, reinterpret_cast<float *>(smem) + kScratchOffset);
+        publish_and_combine(a, R, nsplit, reinterpret_cast<float *>(smem) + (kMulti ? 0 : kScratchOffset));
     } else if (step_check) {                               // one split: its own verdict
         finish_here(false);
     }
     KVQ_STAMP(6);
 }
 
-template <bool kBf16, bool kPrecise, bool kCluster>
+template <bool kBf16, bool kPrecise, bool kCluster, bool kMulti = false>
 cudaError_t configure(int dev)
 {
     static int configured[64] = {0};
     if (dev >= 0 && dev < 64 && configured[dev])
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kBf16, kPrecise, kCluster>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kBf16, kPrecise, kCluster, kMulti>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Tile<kBf16>::kSmemBytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64)
@@ -1133,7 +1221,7 @@ cudaLaunchConfig_t launch_config(const DecodeArgs &a, dim3 grid, cudaStream_t st
     return cfg;
 }
 
-template <bool kBf16, bool kPrecise, bool kCluster>
+template <bool kBf16, bool kPrecise, bool kCluster, bool kMulti>
 cudaError_t launch_split(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                          cudaStream_t stream)
 {
@@ -1141,35 +1229,35 @@ cudaError_t launch_split(const DecodeArgs &a, const CUtensorMap &k_map, const CU
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = configure<kBf16, kPrecise, kCluster>(dev);
+    e = configure<kBf16, kPrecise, kCluster, kMulti>(dev);
     if (e != cudaSuccess)
         return e;
     const dim3 grid(static_cast<unsigned>(a.max_splits),
                     static_cast<unsigned>(a.num_kv_heads * a.row_blocks), static_cast<unsigned>(a.batch));
     cudaLaunchAttribute attr[2];
     const cudaLaunchConfig_t cfg = launch_config<kBf16, kPrecise, kCluster>(a, grid, stream, attr);
-    e = cudaLaunchKernelEx(&cfg, decode_split_kernel<kBf16, kPrecise, kCluster>, k_map, v_map, a);
+    e = cudaLaunchKernelEx(&cfg, decode_split_kernel<kBf16, kPrecise, kCluster, kMulti>, k_map, v_map, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
 }
 
-template <bool kCluster>
+template <bool kCluster, bool kMulti>
 cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                            cudaStream_t stream)
 {
     if (a.bf16_cache)
-        return a.out_fp32 ? launch_split<true, true, kCluster>(a, k_map, v_map, stream)
-                          : launch_split<true, false, kCluster>(a, k_map, v_map, stream);
-    return a.out_fp32 ? launch_split<false, true, kCluster>(a, k_map, v_map, stream)
-                      : launch_split<false, false, kCluster>(a, k_map, v_map, stream);
+        return a.out_fp32 ? launch_split<true, true, kCluster, kMulti>(a, k_map, v_map, stream)
+                          : launch_split<true, false, kCluster, kMulti>(a, k_map, v_map, stream);
+    return a.out_fp32 ? launch_split<false, true, kCluster, kMulti>(a, k_map, v_map, stream)
+                      : launch_split<false, false, kCluster, kMulti>(a, k_map, v_map, stream);
 }
 
-template <bool kBf16>
+template <bool kBf16, bool kMulti>
 int cluster_capacity_query(int n)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || configure<kBf16, false, true>(dev) != cudaSuccess) {
+    if (cudaGetDevice(&dev) != cudaSuccess || configure<kBf16, false, true, kMulti>(dev) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -1179,7 +1267,7 @@ int cluster_capacity_query(int n)
     const cudaLaunchConfig_t cfg =
         launch_config<kBf16, false, true>(a, dim3(static_cast<unsigned>(n), 1, 1), nullptr, attr);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, decode_split_kernel<kBf16, false, true>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_split_kernel<kBf16, false, true, kMulti>, &cfg) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -1194,66 +1282,74 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
 {
     if (a.batch == 0)
         return cudaSuccess;
-#ifdef KVQ_PHASE_STAMPS
-    {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_phase_stamps);
-        if (e == cudaSuccess)
-            e = cudaMemsetAsync(p, 0, sizeof(g_phase_stamps), stream);
-        if (e != cudaSuccess)
-            return e;
-    }
-#endif
-    return a.cluster ? launch_variant<true>(a, k_map, v_map, stream)
-                     : launch_variant<false>(a, k_map, v_map, stream);
+
+    if (a.n_query > 1)                      // several query tokens: the causal, row-blocked build
+        return a.cluster ? launch_variant<true, true>(a, k_map, v_map, stream)
+                         : launch_variant<false, true>(a, k_map, v_map, stream);
+    return a.cluster ? launch_variant<true, false>(a, k_map, v_map, stream)
+                     : launch_variant<false, false>(a, k_map, v_map, stream);
 }
 
-int decode_cluster_capacity(int n, bool bf16_cache)
+int decode_cluster_capacity(int n, bool bf16_cache, bool multi)
 {
     if (n < 2 || n > kMaxCluster)
         return 0;
     static std::mutex mu;
-    static std::map<std::tuple<int, int, bool>, int> cache;
+    static std::map<std::tuple<int, int, bool, bool>, int> cache;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_tuple(dev, n, bf16_cache);
+    const auto key = std::make_tuple(dev, n, bf16_cache, multi);
     auto it = cache.find(key);
     if (it != cache.end())
         return it->second;
-    const int c = bf16_cache ? cluster_capacity_query<true>(n) : cluster_capacity_query<false>(n);
+    const int c = multi ? (bf16_cache ? cluster_capacity_query<true, true>(n) : cluster_capacity_query<false, true>(n))
+                        : (bf16_cache ? cluster_capacity_query<true, false>(n)
+                                      : cluster_capacity_query<false, false>(n));
     cache[key] = c;
     return c;
 }
 
-int decode_ctas_per_sm(bool bf16_cache)
+int decode_ctas_per_sm(bool bf16_cache, bool multi)
 {
-    // resident CTAs per SM as the shared-memory footprint allows (no device)
+    // resident CTAs per SM as the shared-memory footprint and the launch
+    // bounds allow (no device)
     const int by_smem = bf16_cache ? 233472 / (Tile<true>::kSmemBytes + 1024)
                                    : 233472 / (Tile<false>::kSmemBytes + 1024);
-    const int fallback = by_smem < kCtasPerSm ? (by_smem > 0 ? by_smem : 1) : kCtasPerSm;
+    const int bound = multi ? 2 : kCtasPerSm;
+    const int fallback = by_smem < bound ? (by_smem > 0 ? by_smem : 1) : bound;
     static std::mutex mu;
-    static std::map<std::pair<int, bool>, int> cache;
+    static std::map<std::tuple<int, bool, bool>, int> cache;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return fallback;
     }
     std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_pair(dev, bf16_cache);
+    const auto key = std::make_tuple(dev, bf16_cache, multi);
     auto it = cache.find(key);
     if (it != cache.end())
         return it->second;
     int n = 0;
-    cudaError_t e = bf16_cache ? configure<true, false, false>(dev) : configure<false, false, false>(dev);
-    if (e == cudaSuccess)
-        e = bf16_cache ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                             &n, decode_split_kernel<true, false, false>, kThreads, Tile<true>::kSmemBytes)
-                       : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                             &n, decode_split_kernel<false, false, false>, kThreads, Tile<false>::kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    if (multi) {
+        e = bf16_cache ? configure<true, false, false, true>(dev) : configure<false, false, false, true>(dev);
+        if (e == cudaSuccess)
+            e = bf16_cache ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, decode_split_kernel<true, false, false, true>, kThreads, Tile<true>::kSmemBytes)
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, decode_split_kernel<false, false, false, true>, kThreads, Tile<false>::kSmemBytes);
+    } else {
+        e = bf16_cache ? configure<true, false, false>(dev) : configure<false, false, false>(dev);
+        if (e == cudaSuccess)
+            e = bf16_cache ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, decode_split_kernel<true, false, false, false>, kThreads, Tile<true>::kSmemBytes)
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, decode_split_kernel<false, false, false, false>, kThreads, Tile<false>::kSmemBytes);
+    }
     if (e != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = fallback;

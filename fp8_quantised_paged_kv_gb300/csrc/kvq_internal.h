@@ -121,11 +121,16 @@ uint64_t decode_copy_wait_ns();
 // swizzle.
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                           cudaStream_t stream);
-// Resident decode CTAs per SM for the cache type (occupancy of the kernel).
-int decode_ctas_per_sm(bool bf16_cache);
+// Resident decode CTAs per SM for the cache type (occupancy of the kernel;
+// multi: the multi-token build, 16 query rows per CTA).
+int decode_ctas_per_sm(bool bf16_cache, bool multi = false);
 // How many clusters of n split CTAs can be resident at once on the current
 // device (0 if clusters of n cannot be used).
-int decode_cluster_capacity(int n, bool bf16_cache);
+int decode_cluster_capacity(int n, bool bf16_cache, bool multi = false);
+// Query rows one CTA of the multi-token build serves, and the most splits of
+// one of its requests.
+constexpr int kMultiRowsPerCta = 16;
+constexpr int kMultiMaxSplitsPerRequest = 512;
 
 // Box height (in 128-byte rows) of one bulk copy for a page size.
 inline int tma_box_rows(int page_size, bool bf16_cache)

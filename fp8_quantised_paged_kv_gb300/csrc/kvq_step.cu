@@ -85,16 +85,7 @@ cudaError_t launch_tag_check_append(const TagCheckArgs &t, const AppendArgs &a, 
 {
     if (t.batch == 0)
         return cudaSuccess;
-#ifdef KVQ_PHASE_STAMPS
-    {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_check_stamps);
-        if (e == cudaSuccess)
-            e = cudaMemsetAsync(p, 0, sizeof(g_check_stamps), stream);
-        if (e != cudaSuccess)
-            return e;
-    }
-#endif
+
     if (a.bf16_cache)
         tag_check_append_kernel<true><<<static_cast<unsigned>(t.batch), kStepThreads, 0, stream>>>(t, a);
     else
