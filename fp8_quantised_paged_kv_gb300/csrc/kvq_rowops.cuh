@@ -22,6 +22,21 @@ __device__ __forceinline__ bool tag_check_request(const int32_t *block_table,
                                                   int32_t max_pages_per_seq, int32_t page_size,
                                                   int32_t num_pages, int64_t r)
 {
+    const int32_t *bt = block_table + r * max_pages_per_seq;
+    const uint32_t *exp = expected_tags + r * max_pages_per_seq;
+    const int nt = blockDim.x;
+    const int64_t pass = static_cast<int64_t>(nt) * kUnroll;
+    // The first pass's table and expected-tag loads go out together with the
+    // length load (entries of the row past the used ones are read and then
+    // ignored), so the check costs two rounds of dependent loads, not three.
+    int32_t p[kUnroll];
+    uint32_t want[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        const int64_t i = k * nt + threadIdx.x;
+        p[k] = i < max_pages_per_seq ? __ldg(bt + i) : 0;
+        want[k] = i < max_pages_per_seq ? __ldg(exp + i) : 0u;
+    }
     const int64_t len = seq_lens[r] > 0 ? seq_lens[r] : 0;
     int64_t used = (len + page_size - 1) / page_size;
     bool bad = false;
@@ -29,21 +44,20 @@ __device__ __forceinline__ bool tag_check_request(const int32_t *block_table,
         bad = true;
         used = max_pages_per_seq;
     }
-    const int32_t *bt = block_table + r * max_pages_per_seq;
-    const uint32_t *exp = expected_tags + r * max_pages_per_seq;
-    const int nt = blockDim.x;
-    for (int64_t base = 0; base < used; base += static_cast<int64_t>(nt) * kUnroll) {
-        int32_t p[kUnroll];
-        uint32_t want[kUnroll], live[kUnroll];
+    for (int64_t base = 0; base < used; base += pass) {
+        uint32_t live[kUnroll];
+        if (base > 0) {
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            const int64_t i = base + k * nt + threadIdx.x;
-            p[k] = i < used ? __ldg(bt + i) : 0;
-            want[k] = i < used ? __ldg(exp + i) : 0u;
+            for (int k = 0; k < kUnroll; ++k) {
+                const int64_t i = base + k * nt + threadIdx.x;
+                p[k] = i < used ? __ldg(bt + i) : 0;
+                want[k] = i < used ? __ldg(exp + i) : 0u;
+            }
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
-            const bool in_range = p[k] >= 0 && p[k] < num_pages;
+            const int64_t i = base + k * nt + threadIdx.x;
+            const bool in_range = i < used && p[k] >= 0 && p[k] < num_pages;
             live[k] = in_range ? __ldg(page_tags + p[k]) : 0u;
         }
 #pragma unroll
