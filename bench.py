@@ -346,6 +346,10 @@ class Env:
     def event(self):
         return self.torch.cuda.Event(enable_timing=True)
 
+    def flush_l2(self):
+        """Write the 512 MiB buffer: L2 holds none of the next step's data."""
+        self.flush.zero_()
+
     def barrier(self):
         if self.world > 1:
             self.dist.barrier()
@@ -372,7 +376,7 @@ def size_matched_read(env, nbytes, launches=50):
     evs = []
     with torch.cuda.stream(env.stream):
         for i in range(3 + launches):
-            env.flush.zero_()
+            env.flush_l2()
             e0, e1 = env.event(), env.event()
             e0.record(env.stream)
             kvq.kvq_read_probe(src, sink, env.stream)
@@ -395,7 +399,7 @@ def _timed(env, fn, steps, warmup):
     evs = []
     with torch.cuda.stream(env.stream):
         for i in range(warmup + steps):
-            env.flush.zero_()
+            env.flush_l2()
             e0, e1 = env.event(), env.event()
             e0.record(env.stream)
             fn()
@@ -434,7 +438,7 @@ def time_decode_config(env, name, with_cpu=True):
 
     with torch.cuda.stream(st):
         for _ in range(args.warmup):
-            env.flush.zero_()
+            env.flush_l2()
             step()
     # Timed steps: events at the step boundaries only (an event between the
     # launches would stop the attention from starting as a programmatic
@@ -444,7 +448,7 @@ def time_decode_config(env, name, with_cpu=True):
     t0 = time.perf_counter()
     with torch.cuda.stream(st):
         for i in range(args.steps):
-            env.flush.zero_()
+            env.flush_l2()
             evs[i][0].record(st)
             step()
             evs[i][1].record(st)
@@ -457,7 +461,7 @@ def time_decode_config(env, name, with_cpu=True):
     kev = [(env.event(), env.event(), env.event()) for _ in range(args.steps)]
     with torch.cuda.stream(st):
         for i in range(args.steps):
-            env.flush.zero_()
+            env.flush_l2()
             kev[i][0].record(st)
             step(kev[i][1])
             kev[i][2].record(st)
@@ -505,7 +509,7 @@ def time_decode_config(env, name, with_cpu=True):
     e2e = []
     with torch.cuda.stream(st):
         for i in range(args.steps + 2):
-            env.flush.zero_()
+            env.flush_l2()
             e0, e1 = env.event(), env.event()
             e0.record(st)
             dev_buf.copy_(host_buf, non_blocking=True)
@@ -603,7 +607,7 @@ def time_churn(env, with_cpu=True):
             if from_host:
                 host_in.copy_(dev_in)               # this step's inputs, now in host memory
                 torch.cuda.synchronize()
-            env.flush.zero_()
+            env.flush_l2()
             e = [env.event() for _ in range(3)]
             lev = None if layer_rows is None else [(env.event(), env.event()) for _ in range(cd.layers)]
             e[0].record(st)
@@ -723,7 +727,7 @@ def time_handoff(env):
     rows = []
     with torch.cuda.stream(st):
         for i in range(args.warmup + args.steps):
-            env.flush.zero_()
+            env.flush_l2()
             e = [env.event() for _ in range(3)]
             e[0].record(st)
             kvq.kvq_amax_scales(src_desc, ksrc, vsrc, src, ks, vs, st)
@@ -847,7 +851,11 @@ def run_phase_stamps(args):
         rows = []
         with torch.cuda.stream(st):
             for i in range(args.warmup + args.steps):
-                env.flush.zero_()
+                env.flush_l2()
+                # the host synchronises after every step to read the stamps;
+                # keep the GPU busy ~50 us so that the step's launches are all
+                # queued before it runs (as they are in the timed loops)
+                torch.cuda._sleep(100000)
                 fn()
                 torch.cuda.synchronize()
                 if i < args.warmup:

@@ -382,9 +382,11 @@ KVQ_API kvq_status kvq_decode_step(const kvq_cache_desc *desc, const void *q, in
  *   scales         bf16 [N][K/128] (2-byte aligned): one per output column
  *                  and group of 128 consecutive k.
  *   x              bf16 [M][K], 16-byte aligned.  On the tensor cores x and
- *                  the expanded weights are f16: exact for |x| in
- *                  [2^-14, 65504] (as for q in kvq_decode_attn); q is an exact
- *                  f16 integer and the scales apply in fp32.
+ *                  the expanded weights are f16: x is exact for |x| in
+ *                  [2^-14, 65504] and is not range-scaled (unlike q in
+ *                  kvq_decode_attn): |x| above 65504 overflows, below 2^-14
+ *                  loses low bits; q is an exact f16 integer and the scales
+ *                  apply in fp32.
  *   y              [M][N], bf16 or fp32 per out_dtype, 16-byte aligned.
  *   Shapes: K a positive multiple of 256 and at most 65,536; N a multiple of
  *   64 (KVQ_ERR_UNSUPPORTED otherwise); any M >= 0 (16 rows per launch: a
