@@ -54,6 +54,7 @@ PROFILE_SUMMARIES = {                # committed ncu summaries of the decode ker
 W4_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w4a16_m1.json")
 MT_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_mt_uniform8_n4.json")
 MULTI_TOKEN_CONFIGS = ("uniform8",)
+STEADY_STATE_CONFIGS = ("tiny",)
 W4_SOURCES = ("kvq_w4a16.cu", "kvq_ptx.cuh")
 DECODE_CONFIGS = ("tiny", "uniform8", "ragged64", "long4")
 # one layer of the churn workload's shape (64 requests, GQA 32/8, page 16,
@@ -501,6 +502,38 @@ def time_decode_config(env, name, with_cpu=True):
         if mt_prof is not None:
             multi["ncu_n4"] = mt_prof
 
+    # Steady state of a small workload: R steps back to back in one CUDA
+    # graph, step r on its own copy of the cache (the R copies together larger
+    # than L2, so every step reads HBM); per-step time = graph time / R.
+    steady = None
+    if name in STEADY_STATE_CONFIGS:
+        R = 160
+        kc = [dw.k_cache.clone() for _ in range(R)]
+        vc = [dw.v_cache.clone() for _ in range(R)]
+
+        def steady_steps(s_):
+            for r in range(R):
+                kvq.kvq_tag_check_append(dw.desc, dw.block_table, dw.expected_tags, dw.seq_lens,
+                                         dw.page_tags, dw.k_new, dw.v_new, dw.append_slots,
+                                         dw.k_scale, dw.v_scale, kc[r], vc[r], dw.abort, s_)
+                kvq.kvq_decode_attn(dw.desc, dw.q, kc[r], vc[r], dw.k_scale, dw.v_scale,
+                                    dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out, ws,
+                                    args.num_splits, s_)
+        with torch.cuda.stream(st):
+            steady_steps(st)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            steady_steps(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        per_step_ms = _timed(env, graph.replay, 10, 3) / R
+        steady = {"copies_of_the_cache": R, "cache_bytes_total": R * 2 * dw.k_cache.numel(),
+                  "us_per_step": round(per_step_ms * 1e3, 3),
+                  "kv_gbs": round(kv_bytes / (per_step_ms / 1e3) / 1e9, 2),
+                  "how": "one CUDA graph of R back-to-back steps (kvq_tag_check_append, then "
+                         "kvq_decode_attn), step r on cache copy r; L2 flushed before each replay"}
+        del kc, vc, graph
+
     # end to end: the step's inputs (q, new K/V, slots, block table, lengths,
     # expected tags) copied from pinned host memory in one copy, the step,
     # and the output copied back and read on the host
@@ -570,6 +603,7 @@ def time_decode_config(env, name, with_cpu=True):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host_buf.numel(),
                 "d2h_bytes_per_step": out_host.numel() * out_host.element_size()},
         "multi_token": multi,
+        "steady_state_graph": steady,
         "gpu_launches": 2 * args.steps,
         "clocks": env.sampler.summary(t0, t1),
         "device_error_bits": dev_err,

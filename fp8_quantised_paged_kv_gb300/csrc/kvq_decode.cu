@@ -74,7 +74,6 @@ constexpr int kWarps = 4;
 constexpr int kCtasPerSm = 3;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPageList = 8192 / 16 + 8;       // page ids of one split (<= 8192 tokens)
-constexpr int kPrefetchTokens = 256;             // per split, requested into L2 before the wait
 // Published lse of a split that has no result: both are NaN, so the combine
 // zeroes the request either way; the payload tells a failed tag check (the
 // request is aborted and its new token not written) from a copy timeout.
@@ -495,33 +494,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int lines_per_tok = kBf16Cache ? 2 : 1;
 
     // Launched as a programmatic dependent of the previous kernel on the
-    // stream: everything up to the wait overlaps that kernel.  Meanwhile the
-    // split's first kPrefetchTokens tokens are requested into L2, so HBM is
-    // busy before the wait returns.  Values read here only steer those L2
-    // prefetches (hints that L2 keeps coherent with every write): a
-    // block-table entry the previous kernel is still writing costs at most a
-    // useless prefetch.  Everything the split computes with is read after
-    // the wait.
+    // stream (in a decode step: the tag check): the CTA can be resident and
+    // have its tensor maps fetched while that kernel runs, and it reads no
+    // global memory until the wait has returned, that is until the previous
+    // kernel has completed and its writes are visible.  (Asking L2 for the
+    // split's first pages before the wait made the step slower: those
+    // requests compete with the check for the memory system.)
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&k_map);
         prefetch_tensor_map(&v_map);
-    }
-    if (rb == 0) {                                         // the other row blocks read the same pages
-        const int box_tok = ps < kChunkTokens ? ps : kChunkTokens;
-        const int boxes = kPrefetchTokens / box_tok;
-        for (int i = threadIdx.x; i < boxes; i += kThreads) {
-            const int tok = i * box_tok;                   // from the split's start
-            const int pi = tok / ps;
-            if (pi < span) {
-                const int32_t id = __ldcg(bt + pi);       // L2 only: no stale copy in L1
-                if (id >= 0 && id < a.num_pages) {
-                    const int64_t row = (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * ps + tok % ps;
-                    const int32_t y = static_cast<int32_t>(row * lines_per_tok);
-                    tma_prefetch_l2_2d(&k_map, 0, y);
-                    tma_prefetch_l2_2d(&v_map, 0, y);
-                }
-            }
-        }
     }
     grid_dependency_wait();
     KVQ_STAMP(1);

@@ -176,3 +176,38 @@ def test_planner_choices_on_a_host_without_a_gpu(B, hq, ps, maxp, want):
     no clusters): the wave rules for long jobs and the one-wave estimate."""
     st, ms, _ = _plan(ps=ps, hkv=8, B=B, hq=hq, maxp=maxp)
     assert (st, ms) == want
+
+
+def test_multi_token_plan_and_argument_checks():
+    """kvq_decode_plan_mt / kvq_decode_attn_mt on the host: one query token
+    plans exactly as kvq_decode_plan; n tokens need their rows' partials in
+    the workspace and their arrival counters per 16-row block; n outside
+    1..16 is refused before anything reaches a GPU."""
+    desc = kvq.CacheDesc(4104, 16, 8)
+    for splits in (0, 1, 12):
+        assert kvq.kvq_decode_plan_mt(desc, 8, 1, 64, 513, splits) == \
+            kvq.kvq_decode_plan(desc, 8, 64, 513, splits)
+    # 12 splits through the workspace: counters of 8 x 8 x ceil(4 * 8 / 16) blocks,
+    # lse and o of 8 x 4 x 64 rows x 12 splits
+    _, ms, ws = kvq.kvq_decode_plan_mt(desc, 8, 4, 64, 513, 12)
+    assert ms == 12
+    rows = 8 * 4 * 64
+    counters = (8 * 8 * 2 * 4 + 255) // 256 * 256
+    lse = (rows * 12 * 4 + 255) // 256 * 256
+    assert ws == counters + lse + rows * 12 * 128 * 4
+    for n, status in ((0, 1), (17, 2)):
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kvq_decode_plan_mt(desc, 8, n, 64, 513, 0)
+        assert e.value.status == status
+    lib = kvq.load()
+    p = ctypes.c_void_p(0x10000)
+    st = lib.kvq_decode_attn_mt(ctypes.byref(desc.c()), None, 8, 4, 64, p, p, p, p, p, 513, p,
+                                ctypes.c_float(0.1), None, p, 0, p, 1 << 30, 0, None)
+    assert st == 1                                  # null q
+    st = lib.kvq_decode_attn_mt(ctypes.byref(desc.c()), p, 8, 4, 64, p, p, p, p, p, 513, p,
+                                ctypes.c_float(0.1), None, p, 0, p, 16, 12, None)
+    assert st == 3                                  # workspace too small
+    # a request of a multi-token call takes at most 512 splits
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_decode_plan_mt(kvq.CacheDesc(1 << 20, 64, 8), 1, 2, 16, 16384, 1024)
+    assert e.value.status == 2
