@@ -53,3 +53,40 @@ def test_copy_wait_timeout_zeroes_what_it_served_and_recovers(num_splits):
     torch.cuda.synchronize()
     assert kvq.kvq_device_error() == 0
     assert_close(out_to_np(out2), ref, "fp32", "after the limit is restored")
+
+
+@pytest.mark.parametrize("num_splits", [1, 4])
+def test_copy_wait_timeout_in_the_multi_token_build(num_splits):
+    """The same failure path in the multi-token build (its own kernel
+    instantiation): every query row of every (request, KV head) gets zeros,
+    no copy is left in flight, and the next call matches the oracle."""
+    import oracle
+    n = 4
+    w = W.make_custom([4096, 4096, 300, 33], group=4, page_size=16, seed=43)
+    dw = DeviceWorkload(w)
+    dw.append()
+    kc, vc = oracle_caches(dw)
+    q_bits = W.normal_bf16(np.random.default_rng(44), (w.batch, n, w.num_q_heads, w.head_dim))
+    q = torch.from_numpy(q_bits.view(np.int16)).to("cuda").view(torch.bfloat16)
+    ref = oracle.decode_attn_multi(q_bits, kc, vc, dw.k_scale_host, dw.v_scale_host, w.block_table,
+                                   w.seq_lens, w.softmax_scale)
+    ws = kvq.workspace_for_mt(dw.desc, w.batch, n, w.num_q_heads, w.max_pages_per_seq, num_splits)
+    out = torch.full(q.shape, 7.0, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    kvq.kvq_device_error(clear=True)
+    try:
+        kvq.kvq_diag_set_copy_wait_ns(0)
+        kvq.kvq_decode_attn_mt(dw.desc, q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
+                               dw.block_table, dw.seq_lens, w.softmax_scale, None, out, ws, num_splits)
+        torch.cuda.synchronize()
+    finally:
+        kvq.kvq_diag_set_copy_wait_ns(-1)
+    bits = kvq.kvq_device_error(clear=True)
+    assert bits & 1 and not bits & 2
+    assert np.all(out_to_np(out) == 0.0)
+    out2 = torch.empty_like(out)
+    kvq.kvq_decode_attn_mt(dw.desc, q, dw.k_cache, dw.v_cache, dw.k_scale, dw.v_scale,
+                           dw.block_table, dw.seq_lens, w.softmax_scale, None, out2, ws, num_splits)
+    torch.cuda.synchronize()
+    assert kvq.kvq_device_error() == 0
+    assert_close(out_to_np(out2), ref, "fp32", "multi-token, after the limit is restored")
