@@ -14,8 +14,9 @@ Default run (no --workload): every workload, one JSON line.
   layers) / device time of the step.
 
   per_config: tiny, uniform8, ragged64 and long4 (one layer each), timed in
-  the same order: kvq_tag_check_append (the tag check, then the append of
-  each passing request's token), then kvq_decode_attn.  The whole step as
+  the same form as the headline's layer: kvq_tag_check, then
+  kvq_decode_attn_append (the attention with the append of each passing
+  request's new token).  The whole step as
   one kvq_decode_step launch rides along as `one_launch`; it streams a
   split's pages before it learns the split's tag verdict, so it is not the
   timed step.  Every config also carries its BF16-cache step, a plain read
@@ -412,8 +413,8 @@ def _timed(env, fn, steps, warmup):
 
 
 def time_decode_config(env, name, with_cpu=True):
-    """One layer of a decode workload: the step kvq_tag_check_append ->
-    kvq_decode_attn timed over exactly args.steps steps, then the per-kernel
+    """One layer of a decode workload: the step kvq_tag_check ->
+    kvq_decode_attn_append timed over exactly args.steps steps, then the per-kernel
     split, the one-launch step, a plain read of the same bytes, the BF16
     cache, the host-fed step and the CPU oracle's speed."""
     import workloads as W
@@ -432,10 +433,10 @@ def time_decode_config(env, name, with_cpu=True):
                "workspace (last-arriving split)")
 
     def step(mid=None):
-        dw.tag_check_append(st)           # tag check, then the append of each passing request
+        dw.tag_check(st)                  # the batched tag check, its own launch
         if mid is not None:
             mid.record(st)
-        dw.attend(out, ws, dw.abort, args.num_splits, st)
+        dw.attend_append(out, ws, args.num_splits, st)   # attention + append of passing requests
 
     with torch.cuda.stream(st):
         for _ in range(args.warmup):
@@ -513,12 +514,11 @@ def time_decode_config(env, name, with_cpu=True):
 
         def steady_steps(s_):
             for r in range(R):
-                kvq.kvq_tag_check_append(dw.desc, dw.block_table, dw.expected_tags, dw.seq_lens,
-                                         dw.page_tags, dw.k_new, dw.v_new, dw.append_slots,
-                                         dw.k_scale, dw.v_scale, kc[r], vc[r], dw.abort, s_)
-                kvq.kvq_decode_attn(dw.desc, dw.q, kc[r], vc[r], dw.k_scale, dw.v_scale,
-                                    dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort, out, ws,
-                                    args.num_splits, s_)
+                kvq.kvq_tag_check(dw.block_table, dw.expected_tags, dw.seq_lens, w.page_size,
+                                  dw.page_tags, dw.abort, s_)
+                kvq.kvq_decode_attn_append(dw.desc, dw.q, kc[r], vc[r], dw.k_scale, dw.v_scale,
+                                           dw.block_table, dw.seq_lens, w.softmax_scale, dw.abort,
+                                           dw.k_new, dw.v_new, out, ws, args.num_splits, s_)
         with torch.cuda.stream(st):
             steady_steps(st)
         torch.cuda.synchronize()
@@ -530,8 +530,8 @@ def time_decode_config(env, name, with_cpu=True):
         steady = {"copies_of_the_cache": R, "cache_bytes_total": R * 2 * dw.k_cache.numel(),
                   "us_per_step": round(per_step_ms * 1e3, 3),
                   "kv_gbs": round(kv_bytes / (per_step_ms / 1e3) / 1e9, 2),
-                  "how": "one CUDA graph of R back-to-back steps (kvq_tag_check_append, then "
-                         "kvq_decode_attn), step r on cache copy r; L2 flushed before each replay"}
+                  "how": "one CUDA graph of R back-to-back steps (kvq_tag_check, then "
+                         "kvq_decode_attn_append), step r on cache copy r; L2 flushed before each replay"}
         del kc, vc, graph
 
     # end to end: the step's inputs (q, new K/V, slots, block table, lengths,
@@ -564,8 +564,7 @@ def time_decode_config(env, name, with_cpu=True):
         db = DeviceWorkload(w, kvq.KVQ_CACHE_BF16, device=env.dev)
         wsb = db.workspace(args.num_splits)
         ob = db.out(False)
-        bf16_ms = _timed(env, lambda: (db.tag_check_append(st), db.attend(ob, wsb, db.abort,
-                                                                          args.num_splits, st)),
+        bf16_ms = _timed(env, lambda: (db.tag_check(st), db.attend_append(ob, wsb, args.num_splits, st)),
                          args.steps, args.warmup)
         del db, wsb, ob
         torch.cuda.empty_cache()
@@ -576,14 +575,14 @@ def time_decode_config(env, name, with_cpu=True):
                    "head_dim": w.head_dim, "page_size": w.page_size, "cache": "fp8_e4m3",
                    "out": "bf16", "split_tokens": split_tokens, "max_splits": max_splits,
                    "split_combine": combine,
-                   "step": "kvq_tag_check_append, then kvq_decode_attn",
+                   "step": "kvq_tag_check, then kvq_decode_attn_append",
                    "l2": "flushed before every timed step (512 MiB write)"},
         "value": round(agg["value_gbs"], 2), "unit": "GB/s",
         "ms_per_step": round(agg["ms_per_step"], 5),
         "tokens_per_s": round(agg["tokens_per_s"], 1),
         "hbm_frac_of_measured": round(kv_bytes / (agg["ms_per_step"] / 1e3) / 1e9 / env.peak, 4),
-        "kernel_us": {"tag_check_append": round(pre_ms * 1e3, 2),
-                      "decode_attn (split + fused combine)": round(attn_ms * 1e3, 2)},
+        "kernel_us": {"tag_check": round(pre_ms * 1e3, 2),
+                      "decode_attn_append (append + split + fused combine)": round(attn_ms * 1e3, 2)},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(achieved, 1),
                      "peak": env.peak, "unit": "GB/s", "frac": round(achieved / env.peak, 4),
                      "traffic": profiled_traffic(PROFILE_SUMMARIES.get(name), name),
@@ -846,7 +845,8 @@ def run_phase_stamps(args):
     """Where the time of one decode step goes: the library built with
     per-CTA %globaltimer stamps (libkvq_stamps.so) runs the step of a decode
     workload (default uniform8) in three forms -- the conforming two-launch
-    step, the one-launch step and the attention launch alone -- with the L2
+    step (the tag check, then the attention with the append), the one-launch
+    step and the attention launch alone -- with the L2
     flushed before each step; prints, per form, the median over steps of the
     min / median / max over CTAs of each phase's time from the step's first
     CTA entry, in microseconds."""
@@ -874,8 +874,8 @@ def run_phase_stamps(args):
     dec = np.zeros(n_cta * 8, np.uint64)
     chk = np.zeros(w.batch * 2, np.uint64)
     forms = {
-        "two_launch (kvq_tag_check_append, then kvq_decode_attn)":
-            lambda: (dw.tag_check_append(st), dw.attend(out, ws, dw.abort, args.num_splits, st)),
+        "two_launch (kvq_tag_check, then kvq_decode_attn_append)":
+            lambda: (dw.tag_check(st), dw.attend_append(out, ws, args.num_splits, st)),
         "one_launch (kvq_decode_step)": lambda: dw.decode_step(out, ws, args.num_splits, st),
         "attention alone (kvq_decode_attn)":
             lambda: dw.attend(out, ws, dw.abort, args.num_splits, st),
@@ -895,7 +895,7 @@ def run_phase_stamps(args):
                 if i < args.warmup:
                     continue
                 assert lib.kvq_phase_stamps(0, dec.ctypes.data, dec.size) == 0
-                assert lib.kvq_phase_stamps(1, chk.ctypes.data, chk.size) == 0
+                assert lib.kvq_phase_stamps(2, chk.ctypes.data, chk.size) == 0
                 d = dec.reshape(n_cta, 8).astype(np.int64)
                 # nothing is cleared between launches: a CTA that streamed and
                 # finished has an exit stamp later than its entry stamp

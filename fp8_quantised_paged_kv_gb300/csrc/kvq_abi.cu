@@ -713,13 +713,15 @@ kvq_status kvq_diag_set_copy_wait_ns(int64_t ns)
 #ifdef KVQ_PHASE_STAMPS
 // Instrumented build only (no declaration in the public header): copy the
 // phase stamps of the last launch to host memory.  which = 0: decode kernel,
-// [CTA][8]; 1: tag check + append kernel, [CTA][2].
+// [CTA][8]; 1: tag check + append kernel, [CTA][2]; 2: tag check kernel,
+// [CTA][2].
 KVQ_API kvq_status kvq_phase_stamps(int32_t which, unsigned long long *host, size_t count)
 {
     if (host == nullptr)
         return KVQ_ERR_INVALID_ARG;
     return to_status(which == 0 ? kvq::read_decode_stamps(host, count)
-                                : kvq::read_check_stamps(host, count));
+                     : which == 1 ? kvq::read_check_stamps(host, count)
+                                  : kvq::read_tag_stamps(host, count));
 }
 #endif
 

@@ -146,6 +146,7 @@ cudaError_t read_device_error(uint32_t *bits, bool clear);
 // ([CTA][8] points) and of the last tag-check + append launch ([CTA][2]).
 cudaError_t read_decode_stamps(unsigned long long *host, size_t count);
 cudaError_t read_check_stamps(unsigned long long *host, size_t count);
+cudaError_t read_tag_stamps(unsigned long long *host, size_t count);   // tag check alone, [CTA][2]
 #endif
 
 // SMs of the current device, queried once per device.  A host with no usable

@@ -20,14 +20,31 @@ namespace {
 
 constexpr int kTagThreads = 512;
 
+#ifdef KVQ_PHASE_STAMPS
+// Instrumented build only: %globaltimer at entry (point 0) and when the flag
+// is written (1) by thread 0 of every CTA of the last launch.
+constexpr int kTagStampCtas = 4096;
+__device__ unsigned long long g_tag_stamps[kTagStampCtas * 2];
+__device__ __forceinline__ void tag_stamp(int point)
+{
+    if (threadIdx.x == 0 && blockIdx.x < kTagStampCtas)
+        g_tag_stamps[blockIdx.x * 2 + point] = global_timer_ns();
+}
+#define KVQ_TAG_STAMP(p) tag_stamp(p)
+#else
+#define KVQ_TAG_STAMP(p) ((void)0)
+#endif
+
 __global__ void __launch_bounds__(kTagThreads) tag_check_kernel(TagCheckArgs a)
 {
+    KVQ_TAG_STAMP(0);
     grid_launch_dependents();              // a dependent decode launch may begin now
     const int64_t r = blockIdx.x;
     const bool bad = tag_check_request<8>(a.block_table, a.expected_tags, a.seq_lens, a.page_tags,
                                           a.max_pages_per_seq, a.page_size, a.num_pages, r);
     if (threadIdx.x == 0)
         a.abort_flags[r] = bad ? 1 : 0;
+    KVQ_TAG_STAMP(1);
 }
 
 } // namespace
@@ -39,5 +56,13 @@ cudaError_t launch_tag_check(const TagCheckArgs &a, cudaStream_t stream)
     tag_check_kernel<<<static_cast<unsigned>(a.batch), kTagThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
+
+#ifdef KVQ_PHASE_STAMPS
+cudaError_t read_tag_stamps(unsigned long long *host, size_t count)
+{
+    const size_t n = count < static_cast<size_t>(kTagStampCtas * 2) ? count : kTagStampCtas * 2;
+    return cudaMemcpyFromSymbol(host, g_tag_stamps, n * sizeof(unsigned long long));
+}
+#endif
 
 } // namespace kvq

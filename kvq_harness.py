@@ -120,6 +120,14 @@ class DeviceWorkload:
                                    self.v_scale, self.block_table, self.seq_lens,
                                    self.w.softmax_scale, abort, out, workspace, num_splits, stream)
 
+    def attend_append(self, out, workspace, num_splits=0, stream=None):
+        """Attention with the append of each passing request's new token fused
+        in (kvq_decode_attn_append), reading the flags the check wrote."""
+        return kvq.kvq_decode_attn_append(self.desc, self.q, self.k_cache, self.v_cache,
+                                          self.k_scale, self.v_scale, self.block_table,
+                                          self.seq_lens, self.w.softmax_scale, self.abort,
+                                          self.k_new, self.v_new, out, workspace, num_splits, stream)
+
     def tag_check_append(self, stream=None):
         kvq.kvq_tag_check_append(self.desc, self.block_table, self.expected_tags, self.seq_lens,
                                  self.page_tags, self.k_new, self.v_new, self.append_slots,
