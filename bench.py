@@ -482,7 +482,7 @@ def time_decode_config(env, name, with_cpu=True):
         multi = {}
         g = torch.Generator(device=env.dev)
         g.manual_seed(77)
-        for n in (2, 4, 8):
+        for n in (2, 4, 8, 16):
             qn = torch.randn((w.batch, n, w.num_q_heads, w.head_dim), generator=g,
                              device=env.dev).to(torch.bfloat16)
             on = torch.empty_like(qn)
@@ -497,6 +497,9 @@ def time_decode_config(env, name, with_cpu=True):
             multi[n] = {"us": round(ms * 1e3, 2), "kv_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),
                         "frac_of_peak": round(kv_bytes / (ms / 1e3) / 1e9 / env.peak, 4),
                         "query_rows_per_kv_head": n * w.group, "max_splits": plan[1],
+                        # the library's rule: 64 or more rows per KV head over FP8
+                        "kernel": ("tcgen05, operands and accumulators in tensor memory"
+                                   if n * w.group >= 64 else "mma.sync, 16 rows per CTA"),
                         "tokens_per_s": round(w.batch * n / (ms / 1e3), 1)}
             del qn, on, wsn
         mt_prof = profiled_tensor_pipe(MT_PROFILE_SUMMARY, name)

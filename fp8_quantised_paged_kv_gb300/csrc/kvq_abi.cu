@@ -190,13 +190,20 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     if (g > kvq::kMaxGroup)
         return KVQ_ERR_UNSUPPORTED;
     const int64_t max_ctx = static_cast<int64_t>(max_pages) * d->page_size;
-    const int64_t unit = d->page_size > kChunkTokens ? d->page_size : kChunkTokens;
     const bool bf16 = d->cache_dtype == KVQ_CACHE_BF16;
-    // CTAs per split: one per (request, KV head), or with several query
-    // tokens one per (request, KV head, block of 16 query rows)
     const bool multi = n_query > 1;
-    const int64_t row_blocks =
-        multi ? (static_cast<int64_t>(n_query) * g + kvq::kMultiRowsPerCta - 1) / kvq::kMultiRowsPerCta : 1;
+    // Many query rows over an FP8 cache: the tensor-memory kernel, one CTA
+    // per (split, request, KV head) for all n g rows, splits in whole
+    // 64-token tiles, combined through the workspace.
+    const bool umma = kvq::use_umma(bf16, n_query, g);
+    const int64_t min_unit = umma ? kvq::kUmmaTileTokens : kChunkTokens;
+    const int64_t unit = d->page_size > min_unit ? d->page_size : min_unit;
+    // CTAs per split: one per (request, KV head), or in the BF16 multi-token
+    // build one per (request, KV head, block of 16 query rows)
+    const int64_t row_blocks = multi && !umma
+                                   ? (static_cast<int64_t>(n_query) * g + kvq::kMultiRowsPerCta - 1) /
+                                         kvq::kMultiRowsPerCta
+                                   : 1;
     const int64_t pairs = static_cast<int64_t>(batch) * d->num_kv_heads * row_blocks;
     p->row_blocks = static_cast<int32_t>(row_blocks);
     if (static_cast<int64_t>(d->num_kv_heads) * row_blocks > 65535)
@@ -205,6 +212,24 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     bool single_wave = false;
     if (num_splits > 0) {
         want = num_splits;
+    } else if (umma) {
+        // One wave: as many splits as keep every CTA resident at once, each
+        // at least kMinAutoSplitTokens long; a job that needs more than one
+        // wave even with the longest splits takes those.
+        const int64_t slots = static_cast<int64_t>(kvq::device_sm_count()) * kvq::decode_umma_ctas_per_sm();
+        const int64_t jobs = static_cast<int64_t>(batch > 0 ? batch : 1) * d->num_kv_heads;
+        const int64_t big = (max_ctx + kMaxSplitTokens - 1) / kMaxSplitTokens;
+        if (jobs * big >= slots) {
+            want = big;
+        } else {
+            want = slots / jobs;
+            const int64_t most = max_ctx / kMinAutoSplitTokens;
+            if (want > most)
+                want = most;
+            if (want < big)
+                want = big;
+        }
+        single_wave = true;                          // no cluster form
     } else {
         const int64_t slots =
             static_cast<int64_t>(kvq::device_sm_count()) * kvq::decode_ctas_per_sm(bf16, multi);
@@ -240,7 +265,7 @@ kvq_status make_plan(const kvq_cache_desc *d, int32_t batch, int32_t num_q_heads
     // CTAs, the splits merge through distributed shared memory instead of
     // the workspace.
     p->cluster = 0;
-    if (splits >= 2 && batch > 0 &&
+    if (!umma && splits >= 2 && batch > 0 &&
         pairs <= kvq::decode_cluster_capacity(static_cast<int>(splits), bf16, multi))
         p->cluster = static_cast<int32_t>(splits);
     p->counter_bytes = (static_cast<size_t>(pairs) * 4 + 255) / 256 * 256;
@@ -639,6 +664,8 @@ kvq_status kvq_decode_attn_mt(const kvq_cache_desc *desc, const void *q, int32_t
     CUtensorMap km, vm;
     if (!make_cache_map(&km, desc, k_cache) || !make_cache_map(&vm, desc, v_cache))
         return KVQ_ERR_CUDA;
+    if (kvq::use_umma(desc->cache_dtype == KVQ_CACHE_BF16, num_query_tokens, call.args.group))
+        return to_status(kvq::launch_decode_umma(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
     return to_status(kvq::launch_decode(call.args, km, vm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -727,12 +754,14 @@ KVQ_API kvq_status kvq_phase_stamps(int32_t which, unsigned long long *host, siz
 
 kvq_status kvq_device_error(uint32_t *bits, int32_t clear)
 {
-    uint32_t a = 0, b = 0;
+    uint32_t a = 0, b = 0, c = 0;
     cudaError_t e = kvq::read_device_error(&a, clear != 0);
     if (e == cudaSuccess)
         e = kvq::read_w4_error(&b, clear != 0);
+    if (e == cudaSuccess)
+        e = kvq::read_umma_error(&c, clear != 0);
     if (bits)
-        *bits = a | b;
+        *bits = a | b | c;
     return to_status(e);
 }
 

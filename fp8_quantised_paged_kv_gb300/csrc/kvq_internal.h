@@ -132,6 +132,26 @@ int decode_cluster_capacity(int n, bool bf16_cache, bool multi = false);
 constexpr int kMultiRowsPerCta = 16;
 constexpr int kMultiMaxSplitsPerRequest = 512;
 
+// Multi-token decode over an FP8 cache on the 5th-generation tensor cores
+// (tcgen05, accumulators and the A operands in tensor memory): one CTA per
+// (split, KV head, request) takes all n_query * g <= 128 query rows; the
+// splits merge through the workspace (never a cluster).  Split sizes are
+// multiples of kUmmaTileTokens.
+constexpr int kUmmaTileTokens = 64;
+// Query rows per KV head (n_query * g) from which multi-token decode over an
+// FP8 cache takes that kernel; fewer rows take the mma.sync build, which
+// converts K and V per 16 rows but has no tensor-memory pipeline to fill.
+constexpr int kUmmaMinRows = 64;
+inline bool use_umma(bool bf16_cache, int n_query, int group)
+{
+    return !bf16_cache && n_query > 1 && n_query * group >= kUmmaMinRows;
+}
+cudaError_t launch_decode_umma(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                               cudaStream_t stream);
+// Resident CTAs per SM of that kernel (bf16 output; at most 2: tensor memory).
+int decode_umma_ctas_per_sm();
+cudaError_t read_umma_error(uint32_t *bits, bool clear);
+
 // Box height (in 128-byte rows) of one bulk copy for a page size.
 inline int tma_box_rows(int page_size, bool bf16_cache)
 {

@@ -287,9 +287,13 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc *desc, const void *q, in
  *                  kvq_decode_attn.
  *   Every other argument as in kvq_decode_plan / kvq_decode_attn; the
  *   workspace size comes from kvq_decode_plan_mt with the same n.
- * One launch.  A CTA serves up to 8 query rows (token, head) of one (split,
- * request, KV head); when n * g is larger, ceil(n * g / 8) CTAs stream the
- * same pages (each reads them; the copies share them through L2).
+ * One launch.  With an FP8 cache and n * g >= 64 query rows (token, head) per
+ * KV head, one CTA per (split, request, KV head) serves every row on the
+ * 5th-generation tensor cores (tcgen05: Q, P and the accumulators in tensor
+ * memory, K and V converted once to f16 in shared memory); its splits merge
+ * through the workspace and are whole 64-token tiles.  Otherwise a CTA
+ * serves up to 16 query rows, and ceil(n * g / 16) CTAs stream the same pages
+ * (each reads them; the copies share them through L2).
  */
 KVQ_API kvq_status kvq_decode_plan_mt(const kvq_cache_desc *desc, int32_t batch,
                                       int32_t num_query_tokens, int32_t num_q_heads,
@@ -479,6 +483,10 @@ KVQ_API kvq_status kvq_diag_set_copy_wait_ns(int64_t ns);
  *          still land in shared memory that a later CTA uses: results of the
  *          launches made since are undefined; synchronise the device, check
  *          the bits and rerun them.
+ *   Bit 2: in the tensor-core multi-token kernel, a wait for a tensor-core
+ *          step or for another warp's hand-off gave up after its time limit;
+ *          every warp of the CTA gave up with it, the copies in flight were
+ *          waited for, and the requests it served get zeros.
  * 0 means no such event since the last clear.
  */
 KVQ_API kvq_status kvq_device_error(uint32_t *bits, int32_t clear);

@@ -181,20 +181,33 @@ def test_planner_choices_on_a_host_without_a_gpu(B, hq, ps, maxp, want):
 def test_multi_token_plan_and_argument_checks():
     """kvq_decode_plan_mt / kvq_decode_attn_mt on the host: one query token
     plans exactly as kvq_decode_plan; n tokens need their rows' partials in
-    the workspace and their arrival counters per 16-row block; n outside
-    1..16 is refused before anything reaches a GPU."""
+    the workspace, with an arrival counter per 16-row block (mma.sync build),
+    or per (request, KV head) when an FP8 call has 64 or more rows per KV
+    head (the tensor-memory kernel, splits of whole 64-token tiles); n
+    outside 1..16 is refused before anything reaches a GPU."""
     desc = kvq.CacheDesc(4104, 16, 8)
     for splits in (0, 1, 12):
         assert kvq.kvq_decode_plan_mt(desc, 8, 1, 64, 513, splits) == \
             kvq.kvq_decode_plan(desc, 8, 64, 513, splits)
-    # 12 splits through the workspace: counters of 8 x 8 x ceil(4 * 8 / 16) blocks,
-    # lse and o of 8 x 4 x 64 rows x 12 splits
-    _, ms, ws = kvq.kvq_decode_plan_mt(desc, 8, 4, 64, 513, 12)
-    assert ms == 12
     rows = 8 * 4 * 64
-    counters = (8 * 8 * 2 * 4 + 255) // 256 * 256
     lse = (rows * 12 * 4 + 255) // 256 * 256
-    assert ws == counters + lse + rows * 12 * 128 * 4
+    # 4 tokens x 8 heads = 32 rows per KV head: the mma.sync build, counters
+    # of 8 x 8 x ceil(32 / 16) blocks, for either cache type
+    for d in (desc, kvq.CacheDesc(4104, 16, 8, cache_dtype=kvq.KVQ_CACHE_BF16)):
+        _, ms, ws = kvq.kvq_decode_plan_mt(d, 8, 4, 64, 513, 12)
+        assert ms == 12
+        assert ws == (8 * 8 * 2 * 4 + 255) // 256 * 256 + lse + rows * 12 * 128 * 4
+    # 8 tokens x 8 heads = 64 rows over FP8: the tensor-memory kernel, one
+    # CTA (and counter) per (request, KV head), splits of whole 64-token tiles
+    rows8 = 8 * 8 * 64
+    lse8 = (rows8 * 12 * 4 + 255) // 256 * 256
+    st, ms, ws = kvq.kvq_decode_plan_mt(desc, 8, 8, 64, 513, 12)
+    assert ms == 12 and st % 64 == 0
+    assert ws == (8 * 8 * 4 + 255) // 256 * 256 + lse8 + rows8 * 12 * 128 * 4
+    # its automatic plan (host fallback: 152 SMs, one CTA each): uniform8's
+    # shape takes 2 splits of 65 tiles, one wave of 128 CTAs
+    st, ms, _ = kvq.kvq_decode_plan_mt(desc, 8, 8, 64, 513, 0)
+    assert (st, ms) == (4160, 2)
     for n, status in ((0, 1), (17, 2)):
         with pytest.raises(kvq.KvqError) as e:
             kvq.kvq_decode_plan_mt(desc, 8, n, 64, 513, 0)

@@ -61,6 +61,48 @@ def test_multi_token_matches_oracle(n, g, ps, cache):
             assert_close(got, ref, "fp32" if fp32 else "bf16", f"n{n} g{g} ps{ps} {cache} splits{splits}")
 
 
+@pytest.mark.parametrize("n,g,ps", [(8, 8, 16), (16, 4, 32), (16, 8, 16), (11, 6, 64), (13, 5, 128)])
+def test_tensor_memory_kernel_matches_oracle(n, g, ps):
+    """64 or more query rows per KV head over an FP8 cache take the
+    tensor-memory kernel: one CTA per (split, request, KV head) for every row,
+    rows copied across the 128 M slots (66 and 65 rows: not a power of two,
+    so part of the slots are padding), splits of whole 64-token tiles."""
+    w = W.make_custom(LENS, group=g, page_size=ps, seed=n * 100 + g, outlier_frac=0.01)
+    dw = DeviceWorkload(w)
+    dw.append()
+    q_bits, q = _q(w, n, 31 + n)
+    kc, vc = oracle_caches(dw)
+    ref = oracle.decode_attn_multi(q_bits, kc, vc, dw.k_scale_host, dw.v_scale_host, w.block_table,
+                                   w.seq_lens, w.softmax_scale)
+    for splits in (0, 1, 5, 12):
+        for fp32 in (True, False):
+            got = out_to_np(_run(dw, q, n, fp32, splits))
+            assert_close(got, ref, "fp32" if fp32 else "bf16", f"n{n} g{g} ps{ps} splits{splits}")
+
+
+def test_tensor_memory_kernel_zeroed_requests():
+    """The tensor-memory kernel's zero paths: an empty request, a page id out
+    of range, a request longer than its table row and an aborted one get
+    zeros for every row; the others finite output."""
+    n = 16
+    w = W.make_custom([300, 0, 77, 500, 40], group=4, page_size=16, seed=19)
+    w.block_table[2, 1] = w.num_pages + 3
+    w.seq_lens[3] = w.block_table.shape[1] * 16 + 1
+    abort = np.zeros(w.batch, np.uint8)
+    abort[4] = 1
+    dw = DeviceWorkload(w, populate=False)
+    rng = np.random.default_rng(12)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    dw.k_cache.copy_(torch.from_numpy(rng.choice(finite, size=w.cache_shape()).astype(np.uint8)))
+    dw.v_cache.copy_(torch.from_numpy(rng.choice(finite, size=w.cache_shape()).astype(np.uint8)))
+    _, q = _q(w, n, 15)
+    for splits in (1, 0, 4, 12):
+        got = out_to_np(_run(dw, q, n, True, splits, torch.from_numpy(abort).to(DEV)))
+        for r in (1, 2, 3, 4):
+            assert np.all(got[r] == 0.0), (splits, r)
+        assert np.all(np.isfinite(got[0])) and np.any(got[0] != 0)
+
+
 def test_one_query_token_is_kvq_decode_attn():
     w = W.make_custom(LENS, group=8, page_size=16, seed=3)
     dw = DeviceWorkload(w)
@@ -92,11 +134,12 @@ def test_multi_token_zeroed_requests():
         assert np.all(np.isfinite(got[0])) and np.any(got[0] != 0)
 
 
-@pytest.mark.parametrize("n", [2, 4, 8])
+@pytest.mark.parametrize("n", [2, 4, 8, 16])
 def test_uniform8_multi_token_sampled(n):
     """The uniform8 workload (8 x 8,193 tokens, GQA 64/8) with n new query
-    tokens per request: n * 8 query rows per KV head, n CTAs per split
-    streaming the same pages; sampled requests against the oracle."""
+    tokens per request: n * 8 query rows per KV head (the mma.sync build below
+    64 rows, the tensor-memory kernel from 64); sampled requests against the
+    oracle."""
     w = W.make("uniform8")
     dw = DeviceWorkload(w)
     dw.append()                                           # the last position too

@@ -55,13 +55,17 @@ def test_copy_wait_timeout_zeroes_what_it_served_and_recovers(num_splits):
     assert_close(out_to_np(out2), ref, "fp32", "after the limit is restored")
 
 
-@pytest.mark.parametrize("num_splits", [1, 4])
-def test_copy_wait_timeout_in_the_multi_token_build(num_splits):
-    """The same failure path in the multi-token build (its own kernel
-    instantiation): every query row of every (request, KV head) gets zeros,
-    no copy is left in flight, and the next call matches the oracle."""
+@pytest.mark.parametrize("n,num_splits", [(4, 1), (4, 4), (16, 1), (16, 4)])
+def test_copy_wait_timeout_in_the_multi_token_build(n, num_splits):
+    """The same failure path in the multi-token builds: the mma.sync build
+    (4 tokens x 4 heads = 16 rows per KV head) and the tensor-memory kernel
+    (16 x 4 = 64 rows), whose converter warps give up at their first wait,
+    raise the CTA's abort flag so that every other warp's wait gives up too,
+    and whose producer lane drains the copies in flight before the tensor
+    memory is freed.  Every query row of every (request, KV head) gets
+    zeros, no copy is left in flight, and the next call matches the
+    oracle."""
     import oracle
-    n = 4
     w = W.make_custom([4096, 4096, 300, 33], group=4, page_size=16, seed=43)
     dw = DeviceWorkload(w)
     dw.append()
