@@ -54,6 +54,9 @@ PROFILE_SUMMARIES = {                # committed ncu summaries of the decode ker
 }
 W4_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w4a16_m1.json")
 MT_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_mt_uniform8_n4.json")
+# the tensor-memory kernel that takes 64 or more query rows per KV head
+UMMA_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_mt_umma_uniform8_n8.json")
+UMMA_SOURCES = ("kvq_decode_umma.cu", "kvq_umma.cuh", "kvq_ptx.cuh")
 MULTI_TOKEN_CONFIGS = ("uniform8",)
 STEADY_STATE_CONFIGS = ("tiny",)
 W4_SOURCES = ("kvq_w4a16.cu", "kvq_ptx.cuh")
@@ -505,6 +508,9 @@ def time_decode_config(env, name, with_cpu=True):
         mt_prof = profiled_tensor_pipe(MT_PROFILE_SUMMARY, name)
         if mt_prof is not None:
             multi["ncu_n4"] = mt_prof
+        umma_prof = profiled_tensor_pipe(UMMA_PROFILE_SUMMARY, name, UMMA_SOURCES)
+        if umma_prof is not None:
+            multi["ncu_n8"] = umma_prof
 
     # Steady state of a small workload: R steps back to back in one CUDA
     # graph, step r on its own copy of the cache (the R copies together larger
