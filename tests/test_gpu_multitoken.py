@@ -103,6 +103,27 @@ def test_tensor_memory_kernel_zeroed_requests():
         assert np.all(np.isfinite(got[0])) and np.any(got[0] != 0)
 
 
+def test_tensor_memory_kernel_many_splits():
+    """A 70,000-token request with 16 query tokens x 8 heads (128 rows per KV
+    head) in 122 splits: more (row, split) weights than the combine keeps in
+    shared memory, so it computes them from the workspace as it goes.  Against
+    the oracle, and against the same call in 8 splits (weights in the table)."""
+    n = 16
+    w = W.make_custom([70000, 3000], group=8, page_size=16, seed=61)
+    dw = DeviceWorkload(w)
+    dw.append()
+    q_bits, q = _q(w, n, 62)
+    got_many = out_to_np(_run(dw, q, n, True, 128))
+    got_few = out_to_np(_run(dw, q, n, True, 8))
+    plan = kvq.kvq_decode_plan_mt(dw.desc, w.batch, n, w.num_q_heads, w.max_pages_per_seq, 128)
+    assert plan[1] * n * w.group > 8192
+    assert_close(got_many, got_few, "fp32", "122 splits against 8")
+    kc, vc, _, bt, seq = compact_request(dw, 0)
+    ref = oracle.decode_attn_multi(q_bits[0:1], kc, vc, dw.k_scale_host, dw.v_scale_host, bt, seq,
+                                   w.softmax_scale)
+    assert_close(got_many[0:1], ref, "fp32", "70,000 tokens, 122 splits")
+
+
 def test_one_query_token_is_kvq_decode_attn():
     w = W.make_custom(LENS, group=8, page_size=16, seed=3)
     dw = DeviceWorkload(w)
