@@ -660,34 +660,32 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const uint64_t policy = kMulti && a.row_blocks > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
 
 
-    // Issue the copies of this warp's local chunk `it` (lane 0 only).
+    // Issue the copies of this warp's local chunk `it`: the whole warp, one
+    // copy per lane (lanes 0 .. np - 1 the K parts, np .. 2 np - 1 the V
+    // parts), which issues them about twice as fast as one lane in turn.
     auto issue = [&](int it) {
         const int c = warp + it * kWarps;
         const int64_t tok = t0 + static_cast<int64_t>(c) * kChunkTokens;
         const int st = it % T::kStages;
-        uint8_t *kdst = ring + st * T::kStageBytes;
-        uint8_t *vdst = kdst + T::kBytes;
-        int np = 0;
-        int32_t ys[2];
-        for (int part = 0; part < parts; ++part) {
+        const int64_t left = t1 - tok;
+        const int np = left >= kChunkTokens ? parts : static_cast<int>((left + box_tok - 1) / box_tok);
+        if (lane == 0)
+            mbar_arrive_expect_tx(&my_full[st], 2u * part_bytes * np);
+        __syncwarp();
+        if (lane < 2 * np) {
+            const int part = lane < np ? lane : lane - np;
             const int64_t ptok = tok + part * box_tok;
-            if (ptok >= t1)
-                break;
             const int32_t page = page_list[static_cast<int>(ptok / ps) - first_page];
             const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + ptok % ps;
-            ys[np++] = static_cast<int32_t>(row * lines_per_tok);
-        }
-        mbar_arrive_expect_tx(&my_full[st], 2u * part_bytes * np);
-        for (int i = 0; i < np; ++i) {
-            tma_load_2d(kdst + i * part_bytes, &k_map, 0, ys[i], &my_full[st], policy);
-            tma_load_2d(vdst + i * part_bytes, &v_map, 0, ys[i], &my_full[st], policy);
+            uint8_t *dst = ring + st * T::kStageBytes + (lane < np ? 0 : T::kBytes) + part * part_bytes;
+            tma_load_2d(dst, lane < np ? static_cast<const void *>(&k_map) : static_cast<const void *>(&v_map), 0,
+                        static_cast<int32_t>(row * lines_per_tok), &my_full[st], policy);
         }
     };
 
     const int pro = my_chunks < T::kStages ? my_chunks : T::kStages;
-    if (lane == 0)
-        for (int it = 0; it < pro; ++it)
-            issue(it);
+    for (int it = 0; it < pro; ++it)
+        issue(it);
 
     if (step_check) {
         // kvq_decode_step: this split's share of the tag check, its own pages
@@ -1030,7 +1028,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 
         // ---- refill this stage with the chunk kStages ahead
         __syncwarp();
-        if (lane == 0 && it + T::kStages < my_chunks) {
+        if (it + T::kStages < my_chunks) {
             fence_proxy_async_smem();
             issue(it + T::kStages);
         }
