@@ -380,7 +380,9 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPa
 // distributed shared memory:
 //   M = max_s lse_s,  out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).
 // A second barrier keeps every CTA's shared memory alive until its peers
-// have read it.  Every CTA of the cluster calls this exactly once, with the
+// have read it.  It needs no release: a thread reaches it only after the
+// values it loaded from its peers have been consumed by its output stores,
+// and a release there would make every CTA wait for those global stores.  Every CTA of the cluster calls this exactly once, with the
 // same `finisher`: for kvq_decode_step the rank that reads every peer's
 // verdict, else -1.  Returns, on the finisher, whether any split of the
 // request failed its tag check (false elsewhere).
@@ -451,7 +453,8 @@ __device__ bool cluster_finish(const DecodeArgs &a, const Rows<kMulti> &R, Parti
         store_out(a.out, o0 + 2, zero ? 0.f : acc.z / sum, a.out_fp32);
         store_out(a.out, o0 + 3, zero ? 0.f : acc.w / sum, a.out_fp32);
     }
-    cluster_sync();                          // also orders s_any_stale within the CTA
+    __syncthreads();                         // orders s_any_stale within the CTA
+    cluster_sync_relaxed_arrive();           // peers' reads of this CTA's partial are done
     return rank == finisher && s_any_stale != 0;
 }
 
@@ -1129,7 +1132,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     __syncthreads();
     for (int d = threadIdx.x; d < kHeadDim; d += kThreads)
-    for (int h = 0; h < R.nrows; ++h) {
+#pragma unroll
+    for (int h = 0; h < kRowsT; ++h) {
+        if (h >= R.nrows)
+            break;
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
