@@ -367,6 +367,14 @@ __device__ void drop_split(const DecodeArgs &a, const Rows<kMulti> &R, int split
 }
 
 // What a split contributes to the cluster form of the combine.
+// Cluster-wide barrier with a relaxed arrive: it orders no memory access,
+// only the threads' progress (the wait still acquires).
+__device__ __forceinline__ void cluster_sync_relaxed_arrive()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+                 "barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPartialStale = 3 };
 
 // Cluster form of the combine, used when the splits of each (request, KV

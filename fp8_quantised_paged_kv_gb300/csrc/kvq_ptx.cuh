@@ -286,14 +286,6 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Cluster-wide barrier with a relaxed arrive: it orders no memory access,
-// only the threads' progress (the wait still acquires).
-__device__ __forceinline__ void cluster_sync_relaxed_arrive()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
-                 "barrier.cluster.wait.aligned;" ::: "memory");
-}
-
 // Shared-memory address of the same variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local_addr, uint32_t rank)
 {
