@@ -15,12 +15,15 @@
 // converted from e4m3 to f16 once, whatever n is.  The CTA's warps have one
 // job each and hand 64-token tiles to one another through mbarriers:
 //   - warp 8 (producer): tensor copies (TMA, 128-byte swizzle) of the e4m3 K
-//     and V rows of tile j into a 3-stage ring, one copy per lane;
-//   - warps 4..7 (converters): e4m3 -> f16 (exact) into one of two operand
+//     and V rows of tile j into a 4-stage ring, one copy per lane;
+//   - warps 4..7 (converters): e4m3 -> f16 (exact) into one of three operand
 //     buffers, V rows past the split zeroed;
-//   - warp 9, one lane (MMA): S_j = Q K_j^T (M 128 query-row slots, N 64
-//     tokens, K 128) into one of two score buffers in tensor memory, then,
-//     once P_{j-1} is written, O += P_{j-1} V_{j-1} (M 128, N 128, K 64);
+//   - warp 9, one lane: S_j = Q K_j^T (M 128 query-row slots, N 64 tokens,
+//     K 128) into one of two score buffers in tensor memory;
+//   - warp 10, one lane: once P_j is written, O += P_j V_j (M 128, N 128,
+//     K 64).  A tcgen05.mma holds its issuing thread for about 125 cycles
+//     at M 128 and N <= 128, while two issuing warps complete twice as many,
+//     so the two streams go from two warps and overlap;
 //     Q and P are the A operands, read from tensor memory, K and V the B
 //     operands, read from shared memory;
 //   - warps 0..3 (softmax, thread m = tensor-memory lane m): row m of Q
@@ -61,8 +64,9 @@ namespace {
 constexpr int kSoftWarps = 4;                             // warps 0..3: one per tensor-memory lane quarter
 constexpr int kConvWarp0 = kSoftWarps;                    // warps 4..7
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kUThreads = 320;
+constexpr int kMmaWarp = 9;                               // issues S = Q K^T
+constexpr int kPvWarp = 10;                               // issues O += P V
+constexpr int kUThreads = 352;
 constexpr int kTile = 64;                                 // tokens per tile
 constexpr int kStages = 4;                                // e4m3 ring
 constexpr int kStageBytes = 2 * kTile * 128;              // K then V rows of one tile
@@ -80,7 +84,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 64, kColO = 192, kColP = 320, kColPlo = 384;
 constexpr float kRaiseThreshold = 8.f;
 constexpr int kCombineTable = 8192;                       // (row, split) weights the combine keeps in shared memory
-constexpr int kNumBars = 2 * kStages + 2 * kKV + 2 * 2 + 2;   // see the barrier map in the kernel
+constexpr int kNumBars = 2 * kStages + 2 * kKV + 2 * 2 + 3;   // see the barrier map in the kernel
 
 __host__ __device__ constexpr int smem_bytes()
 {
@@ -174,7 +178,7 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
     uint64_t *full_e = bars, *empty_e = bars + kStages;
     uint64_t *conv_full = bars + 2 * kStages, *pv_done = conv_full + kKV;   // per operand buffer
     uint64_t *s_full = pv_done + kKV, *p_full = s_full + 2;                // per score / P buffer
-    uint64_t *q_ready = p_full + 2, *mma_drain = q_ready + 1;
+    uint64_t *q_ready = p_full + 2, *mma_drain = q_ready + 1, *pv_drain = mma_drain + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     int32_t *page_list = reinterpret_cast<int32_t *>(tmem_slot + 4);
     __shared__ int s_abort;
@@ -247,6 +251,7 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
         }
         mbar_init(q_ready, 4);
         mbar_init(mma_drain, 1);
+        mbar_init(pv_drain, 1);
         fence_mbar_init();
     }
     bad = __syncthreads_or(bad);
@@ -331,39 +336,39 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                 uint8_t *kd = sm + kOffKV + kb * kKVBytes;
                 uint8_t *vd = kd + 16384;
                 const int64_t tok0 = t0 + static_cast<int64_t>(j) * kTile;
+                uint4 xk[4], xv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {              // every load of the tile first
+                    const int t = (ct >> 3) + 16 * k;
+                    const uint32_t src = static_cast<uint32_t>(t * 128 + ((c ^ (t & 7)) << 4));
+                    xk[k] = *reinterpret_cast<const uint4 *>(kr + src);
+                    xv[k] = *reinterpret_cast<const uint4 *>(vr + src);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = (ct >> 3) + 16 * k;
-                    const uint32_t src = static_cast<uint32_t>(t * 128 + ((c ^ (t & 7)) << 4));
-                    const uint4 xk = *reinterpret_cast<const uint4 *>(kr + src);
-                    uint4 xv = *reinterpret_cast<const uint4 *>(vr + src);
                     if (tok0 + t >= t1)                    // past the split: V rows must be zero
-                        xv = make_uint4(0u, 0u, 0u, 0u);
+                        xv[k] = make_uint4(0u, 0u, 0u, 0u);
                     const uint32_t base = static_cast<uint32_t>((c >> 2) * 8192);
                     const uint32_t o0 = base + sw128_chunk(t, 2 * (c & 3));
                     const uint32_t o1 = base + sw128_chunk(t, 2 * (c & 3) + 1);
-                    const uint4 k0 = make_uint4(lo16_e4m3x2_to_f16x2(xk.x), hi16_e4m3x2_to_f16x2(xk.x),
-                                                lo16_e4m3x2_to_f16x2(xk.y), hi16_e4m3x2_to_f16x2(xk.y));
-                    const uint4 k1 = make_uint4(lo16_e4m3x2_to_f16x2(xk.z), hi16_e4m3x2_to_f16x2(xk.z),
-                                                lo16_e4m3x2_to_f16x2(xk.w), hi16_e4m3x2_to_f16x2(xk.w));
-                    const uint4 v0 = make_uint4(lo16_e4m3x2_to_f16x2(xv.x), hi16_e4m3x2_to_f16x2(xv.x),
-                                                lo16_e4m3x2_to_f16x2(xv.y), hi16_e4m3x2_to_f16x2(xv.y));
-                    const uint4 v1 = make_uint4(lo16_e4m3x2_to_f16x2(xv.z), hi16_e4m3x2_to_f16x2(xv.z),
-                                                lo16_e4m3x2_to_f16x2(xv.w), hi16_e4m3x2_to_f16x2(xv.w));
+                    const uint4 k0 = make_uint4(lo16_e4m3x2_to_f16x2(xk[k].x), hi16_e4m3x2_to_f16x2(xk[k].x),
+                                                lo16_e4m3x2_to_f16x2(xk[k].y), hi16_e4m3x2_to_f16x2(xk[k].y));
+                    const uint4 k1 = make_uint4(lo16_e4m3x2_to_f16x2(xk[k].z), hi16_e4m3x2_to_f16x2(xk[k].z),
+                                                lo16_e4m3x2_to_f16x2(xk[k].w), hi16_e4m3x2_to_f16x2(xk[k].w));
+                    const uint4 v0 = make_uint4(lo16_e4m3x2_to_f16x2(xv[k].x), hi16_e4m3x2_to_f16x2(xv[k].x),
+                                                lo16_e4m3x2_to_f16x2(xv[k].y), hi16_e4m3x2_to_f16x2(xv[k].y));
+                    const uint4 v1 = make_uint4(lo16_e4m3x2_to_f16x2(xv[k].z), hi16_e4m3x2_to_f16x2(xv[k].z),
+                                                lo16_e4m3x2_to_f16x2(xv[k].w), hi16_e4m3x2_to_f16x2(xv[k].w));
                     // the two slices share banks: the upper half stores its
                     // chunks in the other order, so a store's 8 lanes hit 8
                     // bank groups
-                    if (c < 4) {
-                        *reinterpret_cast<uint4 *>(kd + o0) = k0;
-                        *reinterpret_cast<uint4 *>(kd + o1) = k1;
-                        *reinterpret_cast<uint4 *>(vd + o0) = v0;
-                        *reinterpret_cast<uint4 *>(vd + o1) = v1;
-                    } else {
-                        *reinterpret_cast<uint4 *>(kd + o1) = k1;
-                        *reinterpret_cast<uint4 *>(kd + o0) = k0;
-                        *reinterpret_cast<uint4 *>(vd + o1) = v1;
-                        *reinterpret_cast<uint4 *>(vd + o0) = v0;
-                    }
+                    const bool swap = c >= 4;
+                    const uint32_t oa = swap ? o1 : o0, ob = swap ? o0 : o1;
+                    *reinterpret_cast<uint4 *>(kd + oa) = swap ? k1 : k0;
+                    *reinterpret_cast<uint4 *>(kd + ob) = swap ? k0 : k1;
+                    *reinterpret_cast<uint4 *>(vd + oa) = swap ? v1 : v0;
+                    *reinterpret_cast<uint4 *>(vd + ob) = swap ? v0 : v1;
                 }
                 fence_proxy_async_smem();                  // the writes, for the tensor core;
                 __syncwarp();                              // the ring reads, for the next copy
@@ -373,66 +378,67 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                 }
             }
         } else if (warp == kMmaWarp) {
-            // ------------------------------------------------ MMA issue
+            // ------------------------------------------------ S = Q K^T issue
+            // A tcgen05.mma occupies its issuing thread for about 125 cycles
+            // at these shapes, while two issuing warps complete twice as
+            // many: the two streams (S here, O += P V in warp kPvWarp) go
+            // from two warps and run side by side.
             if (lane == 0) {
-                // descriptors of the first operand buffer's K and V; a k step
-                // or another buffer adds its byte offset / 16 to the start field
+                // descriptor of the first operand buffer's K; a k step or
+                // another buffer adds its byte offset / 16 to the start field
                 const uint64_t dk = umma_desc(smem_addr(sm + kOffKV), 0, 1024);
-                const uint64_t dv = umma_desc(smem_addr(sm + kOffKV + 16384), 8192, 1024);
                 bool ok = wait_or_abort(q_ready, 0, kCopyWaitLimitNs, abort_flag, 4u);
                 if (ok)
                     tmem_fence_after_sync();
-                // Two in-order streams, each issued as soon as it can go: S_js
-                // once tile js is converted and the softmax is done with the
-                // score buffer's previous tile (PV_{js-2} issued); PV_jp once
-                // P_jp is written.
-                int js = 0, jp = 0;
-                uint64_t idle_since = global_timer_ns();
-                while (ok && jp < n_tiles) {
-                    bool progressed = false;
-                    if (js < n_tiles && jp >= js - 1 && mbar_try_wait(&conv_full[js % kKV], (js / kKV) & 1)) {
-                        tmem_fence_after_sync();
-                        const uint64_t dkb = dk + static_cast<uint64_t>(((js % kKV) * kKVBytes) >> 4);
+                for (int js = 0; ok && js < n_tiles; ++js) {
+                    // score buffer js & 1 is free once the softmax has written
+                    // P of tile js - 2 (it read that tile's scores before)
+                    if (js >= 2 && !wait_or_abort(&p_full[js & 1], ((js - 2) >> 1) & 1, kCopyWaitLimitNs,
+                                                  abort_flag, 4u))
+                        break;
+                    if (!wait_or_abort(&conv_full[js % kKV], (js / kKV) & 1, kCopyWaitLimitNs, abort_flag, 4u))
+                        break;
+                    tmem_fence_after_sync();
+                    const uint64_t dkb = dk + static_cast<uint64_t>(((js % kKV) * kKVBytes) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)     // Q: 8 columns (16 dims) per k step
-                            umma_f16_ts(tmem + kColS + 64u * (js & 1), tmem + kColQ + 8u * kk,
-                                        dkb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), kIdescS,
-                                        kk > 0);
-                        umma_commit(&s_full[js & 1]);
-                        ++js;
-                        progressed = true;
-                    }
-                    if (jp < js && mbar_try_wait(&p_full[jp & 1], (jp >> 1) & 1)) {
-                        const int pb = jp & 1, kb = jp % kKV;
-                        tmem_fence_after_sync();
-                        const uint64_t dvb = dv + static_cast<uint64_t>((kb * kKVBytes) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)     // P: 8 columns (16 tokens) per k step
-                            umma_f16_ts(tmem + kColO, tmem + kColP + 32u * pb + 8u * kk,
-                                        dvb + static_cast<uint64_t>(kk * 128), kIdescPV, jp > 0 || kk > 0);
-                        if constexpr (kPrecise) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                umma_f16_ts(tmem + kColO, tmem + kColPlo + 32u * pb + 8u * kk,
-                                            dvb + static_cast<uint64_t>(kk * 128), kIdescPV, true);
-                        }
-                        umma_commit(&pv_done[kb]);
-                        ++jp;
-                        progressed = true;
-                    }
-                    if (progressed) {
-                        idle_since = global_timer_ns();
-                    } else if (*abort_flag) {
-                        ok = false;
-                    } else if (global_timer_ns() - idle_since > kCopyWaitLimitNs) {
-                        *abort_flag = 1;
-                        atomicOr(&g_umma_error, 4u);
-                        ok = false;
-                    }
+                    for (int kk = 0; kk < 8; ++kk)         // Q: 8 columns (16 dims) per k step
+                        umma_f16_ts(tmem + kColS + 64u * (js & 1), tmem + kColQ + 8u * kk,
+                                    dkb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), kIdescS,
+                                    kk > 0);
+                    umma_commit(&s_full[js & 1]);
                 }
                 // nothing this lane issued may still run when the CTA moves on
                 umma_commit(mma_drain);
                 if (!mbar_wait_bounded(mma_drain, 0, kCopyWaitLimitNs))
+                    atomicOr(&g_umma_error, 4u);
+            }
+            __syncwarp();
+        } else if (warp == kPvWarp) {
+            // ------------------------------------------------ O += P V issue
+            if (lane == 0) {
+                const uint64_t dv = umma_desc(smem_addr(sm + kOffKV + 16384), 8192, 1024);
+                for (int jp = 0; jp < n_tiles; ++jp) {
+                    // P of tile jp written (so its scores, hence its K and V
+                    // operands, are complete too)
+                    if (!wait_or_abort(&p_full[jp & 1], (jp >> 1) & 1, kCopyWaitLimitNs, abort_flag, 4u))
+                        break;
+                    const int pb = jp & 1, kb = jp % kKV;
+                    tmem_fence_after_sync();
+                    const uint64_t dvb = dv + static_cast<uint64_t>((kb * kKVBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)         // P: 8 columns (16 tokens) per k step
+                        umma_f16_ts(tmem + kColO, tmem + kColP + 32u * pb + 8u * kk,
+                                    dvb + static_cast<uint64_t>(kk * 128), kIdescPV, jp > 0 || kk > 0);
+                    if constexpr (kPrecise) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f16_ts(tmem + kColO, tmem + kColPlo + 32u * pb + 8u * kk,
+                                        dvb + static_cast<uint64_t>(kk * 128), kIdescPV, true);
+                    }
+                    umma_commit(&pv_done[kb]);
+                }
+                umma_commit(pv_drain);
+                if (!mbar_wait_bounded(pv_drain, 0, kCopyWaitLimitNs))
                     atomicOr(&g_umma_error, 4u);
             }
             __syncwarp();
