@@ -173,7 +173,7 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     // barriers: copy landed / stage free (per ring stage); operands converted,
     // scores ready, P written, O += P V done (per operand / score buffer);
-    // Q staged; the MMA lane's final drain
+    // Q staged; each issuing lane's final drain (S, then O += P V)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDataBytes);
     uint64_t *full_e = bars, *empty_e = bars + kStages;
     uint64_t *conv_full = bars + 2 * kStages, *pv_done = conv_full + kKV;   // per operand buffer
