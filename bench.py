@@ -52,7 +52,10 @@ L2_FLUSH_NOTE = ("flushed before every timed step (a 512 MiB write, then a read 
                  "the timed region)")
 DECODE_SOURCES = ("kvq_decode.cu", "kvq_ptx.cuh")
 PROFILE_SUMMARIES = {                # committed ncu summaries of the decode kernel, by workload
+    "tiny": os.path.join(ROOT, "profiles", "decode_split_tiny.json"),
     "uniform8": os.path.join(ROOT, "profiles", "decode_split_uniform8.json"),
+    "ragged64": os.path.join(ROOT, "profiles", "decode_split_ragged64.json"),
+    "long4": os.path.join(ROOT, "profiles", "decode_split_long4.json"),
     "churn": os.path.join(ROOT, "profiles", "decode_split_churn_layer.json"),
 }
 W4_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w4a16_m1.json")
@@ -603,7 +606,7 @@ def time_decode_config(env, name, with_cpu=True):
                       "decode_attn_append (append + split + fused combine)": round(attn_ms * 1e3, 2)},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(achieved, 1),
                      "peak": env.peak, "unit": "GB/s", "frac": round(achieved / env.peak, 4),
-                     "traffic": profiled_traffic(PROFILE_SUMMARIES.get(name), name),
+                     "traffic": profiled_traffic(PROFILE_SUMMARIES.get(name), name, units=kv_bytes),
                      "peak_kind": env.peak_kind, "algorithmic_bytes_per_launch": kv_bytes,
                      "size_matched_read": smr},
         "one_launch": {"form": "kvq_decode_step (tag check folded into the attention launch: "
