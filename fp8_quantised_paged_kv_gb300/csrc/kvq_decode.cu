@@ -13,16 +13,20 @@
 // group, so each cache byte is fetched from HBM and converted once.  Four
 // warps; each warp owns every 4th 32-token chunk of the split and a private
 // 2-stage ring of shared-memory tiles filled by 2-D tensor bulk copies (TMA,
-// 128-byte swizzle) that an mbarrier per stage tracks; three CTAs fit on an
-// SM, so twelve independent copy streams keep HBM busy.  Per chunk the warp
+// 128-byte swizzle) that an mbarrier per stage tracks, a chunk's copies
+// issued from several lanes at once; three CTAs fit on an SM, so twelve
+// independent copy streams keep HBM busy.  Per chunk the warp
 // runs, on the tensor cores (mma.sync m16n8k16, f16 in, fp32 accumulate),
 // S^T = K Q^T with tokens as M and the g <= 8 query heads as N, an fp32
 // online softmax, and O^T += V^T P^T.  e4m3 codes become f16 in registers
 // (exact); movmatrix turns the score fragment into the PV operand.  The four
 // warps merge in shared memory.  A request that fits in one split gets its
-// output here; otherwise each split publishes (lse, o) and the last split of
-// the (request, KV head) to finish merges them all (the combine), counted by
-// a per-(request, KV head) arrival counter that it resets to zero.
+// output here.  Otherwise the splits merge (the combine) in one of two forms:
+// when every (request, KV head)'s splits can be resident at once as one
+// thread-block cluster, through distributed shared memory after a cluster
+// barrier; else each split publishes (lse, o) to the workspace and the last
+// split of the (request, KV head) to finish merges them all, counted by a
+// per-(request, KV head) arrival counter that it resets to zero.
 #include <cfloat>
 #include <map>
 #include <mutex>
