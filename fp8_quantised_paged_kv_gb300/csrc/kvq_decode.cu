@@ -495,6 +495,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gq = lane >> 2, tq = lane & 3;
     const int g = a.group, ps = a.page_size;
+    const int ps_shift = __ffs(ps) - 1;                  // ps is 16, 32, 64 or 128
     Rows<kMulti> R;
     R.b = b;
     R.kvh = kvh;
@@ -690,8 +691,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         if (lane < 2 * np) {
             const int part = lane < np ? lane : lane - np;
             const int64_t ptok = tok + part * box_tok;
-            const int32_t page = page_list[static_cast<int>(ptok / ps) - first_page];
-            const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + ptok % ps;
+            const int32_t page = page_list[static_cast<int>(ptok >> ps_shift) - first_page];
+            const int64_t row = (static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + (ptok & (ps - 1));
             uint8_t *dst = ring + st * T::kStageBytes + (lane < np ? 0 : T::kBytes) + part * part_bytes;
             tma_load_2d(dst, lane < np ? static_cast<const void *>(&k_map) : static_cast<const void *>(&v_map), 0,
                         static_cast<int32_t>(row * lines_per_tok), &my_full[st], policy);

@@ -188,6 +188,7 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = a.group, R = a.n_query * g, ps = a.page_size;
+    const int ps_shift = __ffs(ps) - 1;                  // ps is 16, 32, 64 or 128
     constexpr int Rp = 2 * kTpc;                           // M slots per copy of the rows
     const int first_page = static_cast<int>(static_cast<int64_t>(split) * a.split_tokens / ps);
     const int span_left = a.max_pages_per_seq - first_page;
@@ -302,13 +303,14 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                 if (lane == 0)
                     mbar_arrive_expect_tx(&full_e[st], static_cast<uint32_t>(2 * np * box_tok * 128));
                 __syncwarp();
-                if (lane < 2 * np) {                       // lane: tensor lane / np, part lane % np
-                    const int part = lane % np;
+                if (lane < 2 * np) {                       // lanes 0 .. np - 1: K parts, np .. 2 np - 1: V parts
+                    const bool is_v = lane >= np;
+                    const int part = is_v ? lane - np : lane;
                     const int64_t ptok = tok + part * box_tok;
-                    const int32_t page = page_list[static_cast<int>(ptok / ps) - first_page];
-                    const int32_t y =
-                        static_cast<int32_t>((static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps + ptok % ps);
-                    uint8_t *dst = sm + kOffRing + st * kStageBytes + (lane / np) * (kTile * 128) +
+                    const int32_t page = page_list[static_cast<int>(ptok >> ps_shift) - first_page];
+                    const int32_t y = static_cast<int32_t>((static_cast<int64_t>(page) * a.num_kv_heads + kvh) * ps +
+                                                           (ptok & (ps - 1)));
+                    uint8_t *dst = sm + kOffRing + st * kStageBytes + (is_v ? kTile * 128 : 0) +
                                    part * box_tok * 128;
                     tma_load_2d(dst, lane < np ? static_cast<const void *>(&k_map) : static_cast<const void *>(&v_map),
                                 0, y, &full_e[st], policy);
