@@ -146,6 +146,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, ui
                                               volatile int *abort_flag, unsigned bit)
 {
     if (limit_ns != 0) {
+        if (mbar_try_wait(bar, parity))                    // already complete: no clock read
+            return true;
         const uint64_t start = global_timer_ns();
         for (uint32_t i = 0; i < (1u << 24); ++i) {
             if (mbar_try_wait_sleep(bar, parity, 200000u))
