@@ -15,8 +15,8 @@
 // converted from e4m3 to f16 once, whatever n is.  The CTA's warps have one
 // job each and hand 64-token tiles to one another through mbarriers:
 //   - warp 8 (producer): tensor copies (TMA, 128-byte swizzle) of the e4m3 K
-//     and V rows of tile j into a 4-stage ring, one copy per lane;
-//   - warps 4..7 (converters): e4m3 -> f16 (exact) into one of three operand
+//     and V rows of tile j into a 5-stage ring, one copy per lane;
+//   - warps 4..7 (converters): e4m3 -> f16 (exact) into one of four operand
 //     buffers, V rows past the split zeroed;
 //   - warp 9, one lane: S_j = Q K_j^T (M 128 query-row slots, N 64 tokens,
 //     K 128) into one of two score buffers in tensor memory;
@@ -68,12 +68,12 @@ constexpr int kMmaWarp = 9;                               // issues S = Q K^T
 constexpr int kPvWarp = 10;                               // issues O += P V
 constexpr int kUThreads = 352;
 constexpr int kTile = 64;                                 // tokens per tile
-constexpr int kStages = 4;                                // e4m3 ring
+constexpr int kStages = 5;                                // e4m3 ring
 constexpr int kStageBytes = 2 * kTile * 128;              // K then V rows of one tile
 constexpr int kOffRing = 0;
 constexpr int kOffKV = kOffRing + kStages * kStageBytes;  // operand buffers: K f16 [64 tok][64 d] x 2, V alike
 constexpr int kKVBytes = 32768;
-constexpr int kKV = 3;                                    // operand buffers in flight
+constexpr int kKV = 4;                                    // operand buffers in flight
 constexpr int kDataBytes = kOffKV + kKV * kKVBytes;
 constexpr int kMergeStride = 132;                         // floats per row of the copies' merge buffer
 constexpr int kMaxPageList = 8192 / 16 + 8;
@@ -356,23 +356,24 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                     const uint32_t base = static_cast<uint32_t>((c >> 2) * 8192);
                     const uint32_t o0 = base + sw128_chunk(t, 2 * (c & 3));
                     const uint32_t o1 = base + sw128_chunk(t, 2 * (c & 3) + 1);
-                    const uint4 k0 = make_uint4(lo16_e4m3x2_to_f16x2(xk[k].x), hi16_e4m3x2_to_f16x2(xk[k].x),
-                                                lo16_e4m3x2_to_f16x2(xk[k].y), hi16_e4m3x2_to_f16x2(xk[k].y));
-                    const uint4 k1 = make_uint4(lo16_e4m3x2_to_f16x2(xk[k].z), hi16_e4m3x2_to_f16x2(xk[k].z),
-                                                lo16_e4m3x2_to_f16x2(xk[k].w), hi16_e4m3x2_to_f16x2(xk[k].w));
-                    const uint4 v0 = make_uint4(lo16_e4m3x2_to_f16x2(xv[k].x), hi16_e4m3x2_to_f16x2(xv[k].x),
-                                                lo16_e4m3x2_to_f16x2(xv[k].y), hi16_e4m3x2_to_f16x2(xv[k].y));
-                    const uint4 v1 = make_uint4(lo16_e4m3x2_to_f16x2(xv[k].z), hi16_e4m3x2_to_f16x2(xv[k].z),
-                                                lo16_e4m3x2_to_f16x2(xv[k].w), hi16_e4m3x2_to_f16x2(xv[k].w));
-                    // the two slices share banks: the upper half stores its
-                    // chunks in the other order, so a store's 8 lanes hit 8
-                    // bank groups
+                    // the two slices share banks: lanes with c >= 4 store their
+                    // two 16-byte chunks in the other order, so a store's 8
+                    // lanes hit 8 bank groups (the words are picked before
+                    // they are converted)
                     const bool swap = c >= 4;
                     const uint32_t oa = swap ? o1 : o0, ob = swap ? o0 : o1;
-                    *reinterpret_cast<uint4 *>(kd + oa) = swap ? k1 : k0;
-                    *reinterpret_cast<uint4 *>(kd + ob) = swap ? k0 : k1;
-                    *reinterpret_cast<uint4 *>(vd + oa) = swap ? v1 : v0;
-                    *reinterpret_cast<uint4 *>(vd + ob) = swap ? v0 : v1;
+                    const uint32_t ka0 = swap ? xk[k].z : xk[k].x, ka1 = swap ? xk[k].w : xk[k].y;
+                    const uint32_t kb0 = swap ? xk[k].x : xk[k].z, kb1 = swap ? xk[k].y : xk[k].w;
+                    const uint32_t va0 = swap ? xv[k].z : xv[k].x, va1 = swap ? xv[k].w : xv[k].y;
+                    const uint32_t vb0 = swap ? xv[k].x : xv[k].z, vb1 = swap ? xv[k].y : xv[k].w;
+                    *reinterpret_cast<uint4 *>(kd + oa) = make_uint4(lo16_e4m3x2_to_f16x2(ka0), hi16_e4m3x2_to_f16x2(ka0),
+                                                                     lo16_e4m3x2_to_f16x2(ka1), hi16_e4m3x2_to_f16x2(ka1));
+                    *reinterpret_cast<uint4 *>(kd + ob) = make_uint4(lo16_e4m3x2_to_f16x2(kb0), hi16_e4m3x2_to_f16x2(kb0),
+                                                                     lo16_e4m3x2_to_f16x2(kb1), hi16_e4m3x2_to_f16x2(kb1));
+                    *reinterpret_cast<uint4 *>(vd + oa) = make_uint4(lo16_e4m3x2_to_f16x2(va0), hi16_e4m3x2_to_f16x2(va0),
+                                                                     lo16_e4m3x2_to_f16x2(va1), hi16_e4m3x2_to_f16x2(va1));
+                    *reinterpret_cast<uint4 *>(vd + ob) = make_uint4(lo16_e4m3x2_to_f16x2(vb0), hi16_e4m3x2_to_f16x2(vb0),
+                                                                     lo16_e4m3x2_to_f16x2(vb1), hi16_e4m3x2_to_f16x2(vb1));
                 }
                 fence_proxy_async_smem();                  // the writes, for the tensor core;
                 __syncwarp();                              // the ring reads, for the next copy
