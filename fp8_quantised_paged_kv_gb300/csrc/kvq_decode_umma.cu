@@ -84,7 +84,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 64, kColO = 192, kColP = 320, kColPlo = 384;
 constexpr float kRaiseThreshold = 8.f;
 constexpr int kCombineTable = 8192;                       // (row, split) weights the combine keeps in shared memory
-constexpr int kNumBars = 2 * kStages + 2 * kKV + 2 * 2 + 3;   // see the barrier map in the kernel
+constexpr int kNumBars = 2 * kStages + 2 * kKV + 3 * 2 + 3;   // see the barrier map in the kernel
 
 __host__ __device__ constexpr int smem_bytes()
 {
@@ -175,12 +175,14 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     // barriers: copy landed / stage free (per ring stage); operands converted,
     // scores ready, P written, O += P V done (per operand / score buffer);
-    // Q staged; each issuing lane's final drain (S, then O += P V)
+    // Q staged; each issuing lane's final drain (S, then O += P V); scores
+    // read (per score buffer)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDataBytes);
     uint64_t *full_e = bars, *empty_e = bars + kStages;
     uint64_t *conv_full = bars + 2 * kStages, *pv_done = conv_full + kKV;   // per operand buffer
     uint64_t *s_full = pv_done + kKV, *p_full = s_full + 2;                // per score / P buffer
     uint64_t *q_ready = p_full + 2, *mma_drain = q_ready + 1, *pv_drain = mma_drain + 1;
+    uint64_t *s_free = pv_drain + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     int32_t *page_list = reinterpret_cast<int32_t *>(tmem_slot + 4);
     __shared__ int s_abort;
@@ -250,6 +252,7 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
             mbar_init(&p_full[i], 4);
         }
         mbar_init(q_ready, 4);
@@ -396,9 +399,9 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                 if (ok)
                     tmem_fence_after_sync();
                 for (int js = 0; ok && js < n_tiles; ++js) {
-                    // score buffer js & 1 is free once the softmax has written
-                    // P of tile js - 2 (it read that tile's scores before)
-                    if (js >= 2 && !wait_or_abort(&p_full[js & 1], ((js - 2) >> 1) & 1, kCopyWaitLimitNs,
+                    // score buffer js & 1 is free once the softmax has read
+                    // the scores of tile js - 2
+                    if (js >= 2 && !wait_or_abort(&s_free[js & 1], ((js - 2) >> 1) & 1, kCopyWaitLimitNs,
                                                   abort_flag, 4u))
                         break;
                     if (!wait_or_abort(&conv_full[js % kKV], (js / kKV) & 1, kCopyWaitLimitNs, abort_flag, 4u))
@@ -540,6 +543,11 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                             p[16 * q + i] = my0 + 16 * q + i < hi ? __uint_as_float(sv[i]) * mul : -INFINITY;
                     }
                 }
+                // the scores are in registers: the buffer can take tile j + 2
+                tmem_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s_free[sb]);
                 float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int i = 0; i < kTpc; ++i)
