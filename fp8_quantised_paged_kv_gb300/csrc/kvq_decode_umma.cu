@@ -524,14 +524,16 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                 const int hi = vl <= my0 ? my0 : (vl >= my0 + kTpc ? my0 + kTpc : static_cast<int>(vl));
                 const uint32_t scol = tmem + lane_base + kColS + 64u * sb + static_cast<uint32_t>(my0);
                 float p[kTpc];
+                const uint64_t mul2 = f2_pack(mul, mul);
                 if (__all_sync(0xFFFFFFFFu, hi == my0 + kTpc)) {   // every column visible: no masks
 #pragma unroll
                     for (int q = 0; q < kTpc / 16; ++q) {
                         uint32_t sv[16];
                         tmem_ld16(scol + 16u * q, sv);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            p[16 * q + i] = __uint_as_float(sv[i]) * mul;
+                        for (int i = 0; i < 16; i += 2)
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), mul2),
+                                      p[16 * q + i], p[16 * q + i + 1]);
                     }
                 } else {
 #pragma unroll
@@ -539,8 +541,12 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                         uint32_t sv[16];
                         tmem_ld16(scol + 16u * q, sv);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            p[16 * q + i] = my0 + 16 * q + i < hi ? __uint_as_float(sv[i]) * mul : -INFINITY;
+                        for (int i = 0; i < 16; i += 2) {
+                            float x0, x1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), mul2), x0, x1);
+                            p[16 * q + i] = my0 + 16 * q + i < hi ? x0 : -INFINITY;
+                            p[16 * q + i + 1] = my0 + 16 * q + i + 1 < hi ? x1 : -INFINITY;
+                        }
                     }
                 }
                 // the scores are in registers: the buffer can take tile j + 2
@@ -581,14 +587,20 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                     m_used = mx;
                 }
                 const float base = m_used == -INFINITY ? 0.f : m_used;
-                float sa[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint64_t nb2 = f2_pack(-base, -base);
+                uint64_t sa2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-                for (int i = 0; i < kTpc; ++i) {
-                    const float ev = fast_exp2(p[i] - base);
-                    p[i] = ev;
-                    sa[i & 3] += ev;
+                for (int i = 0; i < kTpc; i += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_add(f2_pack(p[i], p[i + 1]), nb2), x0, x1);
+                    p[i] = fast_exp2(x0);
+                    p[i + 1] = fast_exp2(x1);
+                    sa2[(i >> 1) & 1] = f2_add(sa2[(i >> 1) & 1], f2_pack(p[i], p[i + 1]));
                 }
-                l_sum += (sa[0] + sa[1]) + (sa[2] + sa[3]);
+                float s0, s1, s2, s3;
+                f2_unpack(sa2[0], s0, s1);
+                f2_unpack(sa2[1], s2, s3);
+                l_sum += (s0 + s1) + (s2 + s3);
                 // P buffer sb is free once O += P V of tile j - 2 is done
                 if (j >= 2 && !__all_sync(0xFFFFFFFFu, wait_or_abort(&pv_done[(j - 2) % kKV], ((j - 2) / kKV) & 1,
                                                                      kCopyWaitLimitNs, abort_flag, 4u)))
