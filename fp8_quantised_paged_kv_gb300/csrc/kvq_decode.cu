@@ -394,9 +394,10 @@ enum PartialStatus { kPartialOk = 0, kPartialEmpty = 1, kPartialInvalid = 2, kPa
 // A second barrier keeps every CTA's shared memory alive until its peers
 // have read it.  It needs no release: a thread reaches it only after the
 // values it loaded from its peers have been consumed by its output stores,
-// and a release there would make every CTA wait for those global stores.  Every CTA of the cluster calls this exactly once, with the
-// same `finisher`: for kvq_decode_step the rank that reads every peer's
-// verdict, else -1.  Returns, on the finisher, whether any split of the
+// and a release there would make every CTA wait for those global stores.
+// Every CTA of the cluster calls this exactly once, with the same
+// `finisher`: for kvq_decode_step the rank that reads every peer's verdict,
+// else -1.  Returns, on the finisher, whether any split of the
 // request failed its tag check (false elsewhere).
 template <bool kMulti>
 __device__ bool cluster_finish(const DecodeArgs &a, const Rows<kMulti> &R, PartialStatus status, float *part,

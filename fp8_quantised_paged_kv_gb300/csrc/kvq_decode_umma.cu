@@ -369,14 +369,18 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
                     const uint32_t kb0 = swap ? xk[k].x : xk[k].z, kb1 = swap ? xk[k].y : xk[k].w;
                     const uint32_t va0 = swap ? xv[k].z : xv[k].x, va1 = swap ? xv[k].w : xv[k].y;
                     const uint32_t vb0 = swap ? xv[k].x : xv[k].z, vb1 = swap ? xv[k].y : xv[k].w;
-                    *reinterpret_cast<uint4 *>(kd + oa) = make_uint4(lo16_e4m3x2_to_f16x2(ka0), hi16_e4m3x2_to_f16x2(ka0),
-                                                                     lo16_e4m3x2_to_f16x2(ka1), hi16_e4m3x2_to_f16x2(ka1));
-                    *reinterpret_cast<uint4 *>(kd + ob) = make_uint4(lo16_e4m3x2_to_f16x2(kb0), hi16_e4m3x2_to_f16x2(kb0),
-                                                                     lo16_e4m3x2_to_f16x2(kb1), hi16_e4m3x2_to_f16x2(kb1));
-                    *reinterpret_cast<uint4 *>(vd + oa) = make_uint4(lo16_e4m3x2_to_f16x2(va0), hi16_e4m3x2_to_f16x2(va0),
-                                                                     lo16_e4m3x2_to_f16x2(va1), hi16_e4m3x2_to_f16x2(va1));
-                    *reinterpret_cast<uint4 *>(vd + ob) = make_uint4(lo16_e4m3x2_to_f16x2(vb0), hi16_e4m3x2_to_f16x2(vb0),
-                                                                     lo16_e4m3x2_to_f16x2(vb1), hi16_e4m3x2_to_f16x2(vb1));
+                    *reinterpret_cast<uint4 *>(kd + oa) =
+                        make_uint4(lo16_e4m3x2_to_f16x2(ka0), hi16_e4m3x2_to_f16x2(ka0),
+                                   lo16_e4m3x2_to_f16x2(ka1), hi16_e4m3x2_to_f16x2(ka1));
+                    *reinterpret_cast<uint4 *>(kd + ob) =
+                        make_uint4(lo16_e4m3x2_to_f16x2(kb0), hi16_e4m3x2_to_f16x2(kb0),
+                                   lo16_e4m3x2_to_f16x2(kb1), hi16_e4m3x2_to_f16x2(kb1));
+                    *reinterpret_cast<uint4 *>(vd + oa) =
+                        make_uint4(lo16_e4m3x2_to_f16x2(va0), hi16_e4m3x2_to_f16x2(va0),
+                                   lo16_e4m3x2_to_f16x2(va1), hi16_e4m3x2_to_f16x2(va1));
+                    *reinterpret_cast<uint4 *>(vd + ob) =
+                        make_uint4(lo16_e4m3x2_to_f16x2(vb0), hi16_e4m3x2_to_f16x2(vb0),
+                                   lo16_e4m3x2_to_f16x2(vb1), hi16_e4m3x2_to_f16x2(vb1));
                 }
                 fence_proxy_async_smem();                  // the writes, for the tensor core;
                 __syncwarp();                              // the ring reads, for the next copy
@@ -543,7 +547,8 @@ decode_mt_umma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_co
 #pragma unroll
                         for (int i = 0; i < 16; i += 2) {
                             float x0, x1;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), mul2), x0, x1);
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), mul2),
+                                      x0, x1);
                             p[16 * q + i] = my0 + 16 * q + i < hi ? x0 : -INFINITY;
                             p[16 * q + i + 1] = my0 + 16 * q + i + 1 < hi ? x1 : -INFINITY;
                         }
